@@ -1,0 +1,94 @@
+// c3_internal.h -- declarations shared by the translation units of libc3.so
+// (host side).  Not installed; the public boundary is include/c3_api.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace c3 {
+
+// One CTA's residency: the SM it ran on and its %globaltimer window.
+struct CtaRec {
+    unsigned int smid;
+    unsigned int used;             // 1 once written
+    unsigned long long t0, t1;
+};
+
+constexpr int kCtaRecs = 256;      // CTAs recorded per kernel (the first 256)
+
+// Device status block (library-owned, reset before each timed run).
+struct DevStatus {
+    int error;                     // 0, or a negative c3_status (first writer wins)
+    int where;                     // code of the wait that gave up
+    int pad0, pad1;
+    unsigned long long gemm_t0;    // min CTA start of the GEMM (%globaltimer, ns)
+    unsigned long long gemm_t1;    // max CTA end
+    unsigned long long comm_t0;    // same for the SM collective
+    unsigned long long comm_t1;
+    unsigned int smid_gemm[8];     // bitmap of SMs that ran a GEMM CTA (256 SMs max)
+    unsigned int smid_comm[8];     // bitmap of SMs that ran a collective CTA
+    CtaRec gemm_rec[kCtaRecs];     // per-CTA residency, indexed by blockIdx.x
+    CtaRec comm_rec[kCtaRecs];
+};
+
+constexpr size_t kStatusBytes = 16384;
+static_assert(sizeof(DevStatus) <= kStatusBytes, "status block too small");
+
+constexpr int kMaxSegs = 64;
+
+// A collective as a list of equal-size byte segments src[i] -> dst[i].
+struct SegTable {
+    const uint8_t* src[kMaxSegs];
+    uint8_t* dst[kMaxSegs];
+    int nseg;
+    int pad;
+    uint64_t seg_bytes;
+};
+
+enum { kSmkVec = 1, kSmkBulk = 2 };
+
+// Per-device state owned by the library.
+struct DeviceState {
+    int device = -1;
+    int sm_count = 0;
+    int l2_bytes = 0;
+    int smem_per_sm = 0;
+    int smem_per_block = 0;
+    int cc_major = 0, cc_minor = 0;
+    cudaStream_t s_gemm = nullptr;     // default priority
+    cudaStream_t s_comm = nullptr;     // default priority
+    cudaStream_t s_comm_hi = nullptr;  // highest priority
+    cudaEvent_t ev[8] = {};
+    DevStatus* status = nullptr;       // device status block
+    bool ready = false;
+};
+
+// Returns the state of the current device, initialising it on first use.
+// nullptr on failure (error text recorded).
+DeviceState* device_state();
+
+// Host-side count of kernels launched (c3_kernel_launches).
+void count_launch();
+
+// Error plumbing (thread-local text for c3_last_error).
+int set_cuda_error(cudaError_t e, const char* what);
+int set_error(int code, const char* what);
+
+// Kernels' host launchers.  Return 0 or a negative c3_status.
+int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                int sm_budget, cudaStream_t s, DevStatus* st, int* ctas_out);
+int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration
+int gemm_init_device();  // function attributes; once per device
+
+int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, cudaStream_t s,
+                   DevStatus* st, int* ctas_out);
+int copy_init_device(int max_reserve);
+int bulk_copy_smem_bytes();
+
+int copy_ce_launch(const SegTable& t, cudaStream_t s);
+
+int status_reset_launch(DevStatus* st, cudaStream_t s);
+int zero_fill_launch(void* buf, size_t bytes, cudaStream_t s);
+
+}  // namespace c3

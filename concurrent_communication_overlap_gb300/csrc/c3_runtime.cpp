@@ -1,0 +1,539 @@
+// c3_runtime.cpp -- host side of libc3.so: the C ABI of include/c3_api.h.
+//
+// Per-device state, argument checks, the four ways of running a GEMM and a
+// collective together (baseline, schedule prioritisation, SM partitioning,
+// copy-engine offload with an optional GEMM SM cap) and the C3 timer.  The
+// modes and the yardstick follow "Optimizing ML Concurrent Computation and
+// Communication with GPU DMA Engines" as its review pages state them:
+//   ideal speedup    = (T_gemm + T_comm) / max(T_gemm, T_comm), isolated times
+//                      (abstract; referee report summary; Section IV-B3);
+//   c3_sp            = communication kernel scheduled first, at high priority
+//                      ("If this is right": schedule the lower-workgroup-count
+//                      kernel first);
+//   c3_rp            = disjoint compute-unit budgets (Section V-B);
+//   ConCCL / _rp     = the collective on DMA engines, optionally with compute
+//                      units taken from the GEMM (Sections VI-B, VI-F).
+// The pages call the achieved fraction "% of ideal speedup"; this library
+// reports both readings of it: the share of the ideal gain realized,
+// (S_real - 1) / (S_ideal - 1), and the ratio S_real / S_ideal.
+#include "../../include/c3_api.h"
+#include "c3_internal.h"
+
+#include <atomic>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <thread>
+
+namespace c3 {
+
+static thread_local char g_err[512] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int set_cuda_error(cudaError_t e, const char* what) {
+    std::snprintf(g_err, sizeof g_err, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    cudaGetLastError();  // clear the sticky-free error so later calls are not blamed
+    return C3_ECUDA;
+}
+
+int set_error(int code, const char* what) {
+    std::snprintf(g_err, sizeof g_err, "%s", what);
+    return code;
+}
+
+constexpr int kMaxDevices = 64;
+static DeviceState g_dev[kMaxDevices];
+
+static int init_device(DeviceState& ds, int dev) {
+    ds.device = dev;
+    cudaError_t e;
+#define C3_TRY(call, what)                                \
+    do {                                                  \
+        e = (call);                                       \
+        if (e != cudaSuccess) return set_cuda_error(e, what); \
+    } while (0)
+    C3_TRY(cudaDeviceGetAttribute(&ds.sm_count, cudaDevAttrMultiProcessorCount, dev), "sm count");
+    C3_TRY(cudaDeviceGetAttribute(&ds.l2_bytes, cudaDevAttrL2CacheSize, dev), "l2 size");
+    C3_TRY(cudaDeviceGetAttribute(&ds.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
+           "smem per sm");
+    C3_TRY(cudaDeviceGetAttribute(&ds.smem_per_block, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+           "smem per block");
+    C3_TRY(cudaDeviceGetAttribute(&ds.cc_major, cudaDevAttrComputeCapabilityMajor, dev), "cc major");
+    C3_TRY(cudaDeviceGetAttribute(&ds.cc_minor, cudaDevAttrComputeCapabilityMinor, dev), "cc minor");
+    if (ds.cc_major != 10 || ds.cc_minor != 3)
+        return set_error(C3_EUNSUP, "libc3 is built for sm_103a (GB300) only");
+    if (ds.sm_count > 256) return set_error(C3_EUNSUP, "more than 256 SMs: %smid maps hold 256");
+    int lo = 0, hi = 0;
+    C3_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi), "stream priority range");
+    C3_TRY(cudaStreamCreateWithPriority(&ds.s_gemm, cudaStreamNonBlocking, lo), "stream");
+    C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm, cudaStreamNonBlocking, lo), "stream");
+    C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
+    for (auto& ev : ds.ev) C3_TRY(cudaEventCreate(&ev), "event");
+    C3_TRY(cudaMalloc(reinterpret_cast<void**>(&ds.status), kStatusBytes), "status block");
+    C3_TRY(cudaMemset(ds.status, 0, kStatusBytes), "status block");
+#undef C3_TRY
+    int rc = gemm_init_device();
+    if (rc) return rc;
+    rc = copy_init_device(ds.smem_per_block);
+    if (rc) return rc;
+    ds.ready = true;
+    return 0;
+}
+
+static void release_device(DeviceState& ds) {
+    if (ds.s_gemm) cudaStreamDestroy(ds.s_gemm);
+    if (ds.s_comm) cudaStreamDestroy(ds.s_comm);
+    if (ds.s_comm_hi) cudaStreamDestroy(ds.s_comm_hi);
+    for (auto& ev : ds.ev)
+        if (ev) cudaEventDestroy(ev);
+    if (ds.status) cudaFree(ds.status);
+    ds = DeviceState();
+}
+
+DeviceState* device_state() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "cudaGetDevice");
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_error(C3_EUNSUP, "device ordinal out of range");
+        return nullptr;
+    }
+    DeviceState& ds = g_dev[dev];
+    if (!ds.ready) {
+        int rc = init_device(ds, dev);
+        if (rc) {
+            release_device(ds);
+            return nullptr;
+        }
+    }
+    return &ds;
+}
+
+static int default_comm_sms(const DeviceState& ds) {
+    // About a fifth of the SMs: the share the pages' library gives its
+    // all-gather kernel by default (64 of 304 compute units, Figure 5 caption).
+    int k = (ds.sm_count * 64 + 303) / 304;
+    return k < 1 ? 1 : k;
+}
+
+// Shared memory a partitioned collective CTA reserves so that neither a GEMM
+// CTA nor a second collective CTA fits on its SM.
+static int exclusive_reserve(const DeviceState& ds) {
+    int need_vs_gemm = ds.smem_per_sm - gemm_smem_bytes() + 1024;
+    int need_vs_self = ds.smem_per_sm / 2 + 1024;
+    int r = need_vs_gemm > need_vs_self ? need_vs_gemm : need_vs_self;
+    return r > ds.smem_per_block ? ds.smem_per_block : r;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return na && nb && x < y + nb && y < x + na;
+}
+
+static int check_gemm(const void* A, const void* B, const float* C, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return set_error(C3_EINVAL, "negative GEMM dimension");
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF)
+        return set_error(C3_EUNSUP, "GEMM dimension above 2^31-1");
+    if (M == 0 || N == 0) return C3_OK;
+    if (!C) return set_error(C3_EINVAL, "C is NULL");
+    if (!aligned16(C)) return set_error(C3_EALIGN, "C must be 16-byte aligned");
+    if (K == 0) return C3_OK;
+    if (!A || !B) return set_error(C3_EINVAL, "A or B is NULL");
+    if (!aligned16(A) || !aligned16(B)) return set_error(C3_EALIGN, "A and B must be 16-byte aligned");
+    if (K % 8) return set_error(C3_EALIGN, "K must be a multiple of 8 (16-byte TMA row pitch)");
+    return C3_OK;
+}
+
+static int build_allgather(const void* const* shards, void* out, size_t shard_bytes, int nranks,
+                           SegTable* t) {
+    if (nranks < 1 || nranks > kMaxSegs) return set_error(C3_EINVAL, "nranks must be 1..64");
+    if (!shards || !out) return set_error(C3_EINVAL, "shards or out is NULL");
+    if (shard_bytes % 16) return set_error(C3_EALIGN, "shard_bytes must be a multiple of 16");
+    if (!aligned16(out)) return set_error(C3_EALIGN, "out must be 16-byte aligned");
+    std::memset(t, 0, sizeof *t);
+    for (int r = 0; r < nranks; ++r) {
+        if (!shards[r]) return set_error(C3_EINVAL, "a shard pointer is NULL");
+        if (!aligned16(shards[r])) return set_error(C3_EALIGN, "shards must be 16-byte aligned");
+        if (overlaps(shards[r], shard_bytes, out, shard_bytes * (size_t)nranks))
+            return set_error(C3_EINVAL, "out overlaps a shard");
+        t->src[r] = static_cast<const uint8_t*>(shards[r]);
+        t->dst[r] = static_cast<uint8_t*>(out) + (size_t)r * shard_bytes;
+    }
+    t->nseg = nranks;
+    t->seg_bytes = shard_bytes;
+    return C3_OK;
+}
+
+static int build_alltoall(const void* in, void* out, size_t block_bytes, int nranks, SegTable* t) {
+    if (nranks < 1 || nranks * nranks > kMaxSegs) return set_error(C3_EINVAL, "nranks must be 1..8");
+    if (!in || !out) return set_error(C3_EINVAL, "in or out is NULL");
+    if (block_bytes % 16) return set_error(C3_EALIGN, "block_bytes must be a multiple of 16");
+    if (!aligned16(in) || !aligned16(out)) return set_error(C3_EALIGN, "in and out must be 16-byte aligned");
+    const size_t total = block_bytes * (size_t)nranks * (size_t)nranks;
+    if (overlaps(in, total, out, total)) return set_error(C3_EINVAL, "in and out overlap");
+    std::memset(t, 0, sizeof *t);
+    for (int i = 0; i < nranks; ++i)
+        for (int j = 0; j < nranks; ++j) {
+            t->src[i * nranks + j] = static_cast<const uint8_t*>(in) + (size_t)(i * nranks + j) * block_bytes;
+            t->dst[i * nranks + j] = static_cast<uint8_t*>(out) + (size_t)(j * nranks + i) * block_bytes;
+        }
+    t->nseg = nranks * nranks;
+    t->seg_bytes = block_bytes;
+    return C3_OK;
+}
+
+// One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
+// the CTAs keep their SMs to themselves (partitioning).
+static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int budget,
+                       bool exclusive, cudaStream_t s, int* ctas) {
+    if (ctas) *ctas = 0;
+    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, s);
+    int k = budget > 0 ? budget : default_comm_sms(ds);
+    if (k > ds.sm_count) k = ds.sm_count;
+    int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
+                  : sm_kernel == C3_SMK_BULK ? kSmkBulk
+                  : (exclusive ? kSmkBulk : kSmkVec);
+    int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
+    return copy_sm_launch(t, k, flavour, reserve, s, ds.status, ctas);
+}
+
+static int wait_event(cudaEvent_t ev, double limit_s) {
+    auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return C3_OK;
+        if (e != cudaErrorNotReady) return set_cuda_error(e, "waiting for a run");
+        double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+        if (el > limit_s) return set_error(C3_ETIMEOUT, "host wait for the run exceeded its limit");
+        std::this_thread::yield();
+    }
+}
+
+static double elapsed_s(cudaEvent_t a, cudaEvent_t b) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, a, b) != cudaSuccess) return -1.0;
+    return (double)ms * 1e-3;
+}
+
+static int popcount8(const unsigned int* m) {
+    int n = 0;
+    for (int i = 0; i < 8; ++i) n += __builtin_popcount(m[i]);
+    return n;
+}
+
+// SMs on which a GEMM CTA and a collective CTA were resident at the same
+// time (their %globaltimer windows intersect), from the residency records.
+static int coresident_sms(const DevStatus& h, int* shared_any) {
+    unsigned int both_time[8] = {0}, both_any[8] = {0};
+    for (int g = 0; g < kCtaRecs; ++g) {
+        const CtaRec& a = h.gemm_rec[g];
+        if (!a.used) continue;
+        for (int c = 0; c < kCtaRecs; ++c) {
+            const CtaRec& b = h.comm_rec[c];
+            if (!b.used || a.smid != b.smid || a.smid >= 256) continue;
+            both_any[a.smid >> 5] |= 1u << (a.smid & 31);
+            if (a.t0 < b.t1 && b.t0 < a.t1) both_time[a.smid >> 5] |= 1u << (a.smid & 31);
+        }
+    }
+    *shared_any = popcount8(both_any);
+    return popcount8(both_time);
+}
+
+// Reads the status block into `out` (device windows, SM facts) and returns
+// the device error word.
+static int read_status(DeviceState& ds, c3_timing* out) {
+    static DevStatus h;  // 12+ KiB: not on the stack
+    cudaError_t e = cudaMemcpy(&h, ds.status, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_cuda_error(e, "reading the status block");
+    if (out) {
+        out->t_gemm_dev = (h.gemm_t1 > h.gemm_t0) ? (double)(h.gemm_t1 - h.gemm_t0) * 1e-9 : 0.0;
+        out->t_comm_dev = (h.comm_t1 > h.comm_t0) ? (double)(h.comm_t1 - h.comm_t0) * 1e-9 : 0.0;
+        out->gemm_sms = popcount8(h.smid_gemm);
+        out->comm_sms = popcount8(h.smid_comm);
+        out->smid_overlap = coresident_sms(h, &out->sms_shared_any);
+    }
+    if (h.error) {
+        char buf[128];
+        std::snprintf(buf, sizeof buf, "device wait gave up (site %d)", h.where);
+        return set_error(h.error, buf);
+    }
+    return C3_OK;
+}
+
+static int check_problem(const c3_problem* p, SegTable* t) {
+    if (!p) return set_error(C3_EINVAL, "problem is NULL");
+    int rc = check_gemm(p->A, p->B, p->C, p->M, p->N, p->K);
+    if (rc) return rc;
+    if (p->coll == C3_COLL_ALLGATHER)
+        rc = build_allgather(p->shards, p->recv, p->unit_bytes, p->nranks, t);
+    else if (p->coll == C3_COLL_ALLTOALL)
+        rc = build_alltoall(p->send, p->recv, p->unit_bytes, p->nranks, t);
+    else
+        return set_error(C3_EINVAL, "unknown collective");
+    if (rc) return rc;
+    if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
+    if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
+    if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
+    const size_t cb = t->seg_bytes * (size_t)t->nseg;
+    if (overlaps(p->C, (size_t)p->M * (size_t)p->N * 4, p->recv, cb))
+        return set_error(C3_EINVAL, "C overlaps the collective's output");
+    return C3_OK;
+}
+
+// One run of `mode` on already-checked arguments; fills t_conc, the event
+// times and the device facts.
+static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int mode, int sm_split,
+                    int priority, c3_timing* out) {
+    cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
+    cudaEvent_t ev0 = ds.ev[0], ev_g = ds.ev[1], ev_c = ds.ev[2], ev_end = ds.ev[3];
+    int rc = status_reset_launch(ds.status, s0);
+    if (rc) return rc;
+    cudaError_t e;
+    int gctas = 0, cctas = 0;
+    const bool serial = (mode == C3_MODE_SERIAL_SM || mode == C3_MODE_SERIAL_CE);
+    const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
+    if ((e = cudaEventRecord(ev0, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    if (serial) {
+        rc = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds.status, &gctas);
+        if (rc) return rc;
+        if ((e = cudaEventRecord(ev_g, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+        rc = launch_coll(ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, &cctas);
+        if (rc) return rc;
+        if ((e = cudaEventRecord(ev_c, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    } else {
+        if (sm_split < 0 || sm_split >= ds.sm_count)
+            return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
+        cudaStream_t sg = ds.s_gemm;
+        cudaStream_t sc = priority ? ds.s_comm_hi : ds.s_comm;
+        if ((e = cudaStreamWaitEvent(sg, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        const int gemm_budget = sm_split > 0 ? ds.sm_count - sm_split : 0;
+        const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
+        const int comm_budget = part ? sm_split : p->comm_sms;
+        auto go_gemm = [&] { return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, gemm_budget, sg, ds.status, &gctas); };
+        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, comm_budget, part, sc, &cctas); };
+        if (priority) {
+            if ((rc = go_comm())) return rc;
+            if ((rc = go_gemm())) return rc;
+        } else {
+            if ((rc = go_gemm())) return rc;
+            if ((rc = go_comm())) return rc;
+        }
+        if ((e = cudaEventRecord(ev_g, sg)) != cudaSuccess) return set_cuda_error(e, "event record");
+        if ((e = cudaEventRecord(ev_c, sc)) != cudaSuccess) return set_cuda_error(e, "event record");
+        if ((e = cudaStreamWaitEvent(s0, ev_g, 0)) != cudaSuccess) return set_cuda_error(e, "join");
+        if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
+    }
+    if ((e = cudaEventRecord(ev_end, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    if ((rc = wait_event(ev_end, 120.0))) return rc;
+    out->t_conc = elapsed_s(ev0, ev_end);
+    out->t_gemm_ev = elapsed_s(ev0, ev_g);
+    out->t_comm_ev = elapsed_s(ev0, ev_c);
+    out->gemm_ctas = gctas;
+    out->comm_ctas = cctas;
+    return read_status(ds, out);
+}
+
+// Times one phase that runs entirely on `s0`: fn() enqueues it.
+template <class F>
+static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, double* t_out, F fn) {
+    int rc;
+    if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
+    cudaError_t e;
+    if ((e = cudaEventRecord(ds.ev[4], s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    if ((rc = fn())) return rc;
+    if ((e = cudaEventRecord(ds.ev[5], s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    if ((rc = wait_event(ds.ev[5], 120.0))) return rc;
+    *t_out = elapsed_s(ds.ev[4], ds.ev[5]);
+    return C3_OK;
+}
+
+static void fill_metrics(c3_timing* r) {
+    r->t_serial = r->t_gemm_iso + r->t_comm_iso;
+    r->t_ideal = r->t_gemm_iso > r->t_comm_iso ? r->t_gemm_iso : r->t_comm_iso;
+    r->s_ideal = r->t_ideal > 0 ? r->t_serial / r->t_ideal : 0.0;
+    r->s_real = r->t_conc > 0 ? r->t_serial / r->t_conc : 0.0;
+    r->pct_ideal_gain = r->s_ideal > 1.0 ? (r->s_real - 1.0) / (r->s_ideal - 1.0) : 0.0;
+    r->pct_ideal_ratio = r->s_ideal > 0 ? r->s_real / r->s_ideal : 0.0;
+    if (r->t_gemm_iso >= 1.15 * r->t_comm_iso)
+        r->cls = C3_CLASS_G_LONG;
+    else if (r->t_comm_iso >= 1.15 * r->t_gemm_iso)
+        r->cls = C3_CLASS_C_LONG;
+    else
+        r->cls = C3_CLASS_GC_EQUAL;
+}
+
+}  // namespace c3
+
+using namespace c3;
+
+extern "C" {
+
+const char* c3_strerror(int status) {
+    switch (status) {
+        case C3_OK: return "ok";
+        case C3_EINVAL: return "invalid argument";
+        case C3_EALIGN: return "misaligned pointer or size";
+        case C3_ECUDA: return "CUDA error";
+        case C3_ETIMEOUT: return "bounded wait timed out";
+        case C3_EUNSUP: return "unsupported";
+        default: return "unknown status";
+    }
+}
+
+const char* c3_last_error(void) { return g_err; }
+
+uint64_t c3_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int c3_get_device_info(c3_device_info* out) {
+    if (!out) return set_error(C3_EINVAL, "out is NULL");
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    out->device = ds->device;
+    out->sm_count = ds->sm_count;
+    out->l2_bytes = ds->l2_bytes;
+    out->smem_per_sm = ds->smem_per_sm;
+    out->smem_per_block = ds->smem_per_block;
+    out->cc_major = ds->cc_major;
+    out->cc_minor = ds->cc_minor;
+    out->gemm_smem_bytes = gemm_smem_bytes();
+    out->comm_default_sms = default_comm_sms(*ds);
+    return C3_OK;
+}
+
+int c3_status_check(c3_stream s) {
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");
+    int rc = read_status(*ds, nullptr);
+    e = cudaMemset(ds->status, 0, kStatusBytes);
+    if (e != cudaSuccess) return set_cuda_error(e, "clearing the status block");
+    return rc;
+}
+
+int c3_shutdown(void) {
+    for (auto& ds : g_dev)
+        if (ds.ready) {
+            int cur = 0;
+            cudaGetDevice(&cur);
+            cudaSetDevice(ds.device);
+            cudaDeviceSynchronize();
+            release_device(ds);
+            cudaSetDevice(cur);
+        }
+    return C3_OK;
+}
+
+int c3_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
+            c3_stream s) {
+    int rc = check_gemm(A, B, C, M, N, K);
+    if (rc) return rc;
+    if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
+    if (M == 0 || N == 0) return C3_OK;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    return gemm_launch(A, B, C, M, N, K, sm_budget, static_cast<cudaStream_t>(s), ds->status, nullptr);
+}
+
+int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int nranks, int engine,
+                 int sm_budget, c3_stream s) {
+    if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");
+    if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
+    SegTable t;
+    int rc = build_allgather(shards, out, shard_bytes, nranks, &t);
+    if (rc) return rc;
+    if (shard_bytes == 0) return C3_OK;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+}
+
+int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int engine, int sm_budget,
+                c3_stream s) {
+    if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");
+    if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
+    SegTable t;
+    int rc = build_alltoall(in, out, block_bytes, nranks, &t);
+    if (rc) return rc;
+    if (block_bytes == 0) return C3_OK;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+}
+
+int c3_l2_flush(void* buf, size_t bytes, c3_stream s) {
+    if (!buf && bytes) return set_error(C3_EINVAL, "buf is NULL");
+    if (!aligned16(buf)) return set_error(C3_EALIGN, "buf must be 16-byte aligned");
+    return zero_fill_launch(buf, bytes, static_cast<cudaStream_t>(s));
+}
+
+int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing* out) {
+    if (!out) return set_error(C3_EINVAL, "out is NULL");
+    std::memset(out, 0, sizeof *out);
+    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
+    if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
+    SegTable t;
+    int rc = check_problem(p, &t);
+    if (rc) return rc;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
+    out->mode = mode;
+    out->sm_split = sm_split;
+    out->priority = priority;
+    rc = run_once(*ds, p, t, mode, sm_split, priority, out);
+    out->status = rc;
+    return rc;
+}
+
+int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmup, int reps,
+            c3_timing* per_rep) {
+    if (!per_rep || reps < 1 || warmup < 0) return set_error(C3_EINVAL, "need reps >= 1, warmup >= 0, per_rep");
+    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
+    if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
+    SegTable t;
+    int rc = check_problem(p, &t);
+    if (rc) return rc;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
+    cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
+    const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
+    for (int it = 0; it < warmup + reps; ++it) {
+        c3_timing r;
+        std::memset(&r, 0, sizeof r);
+        rc = time_phase(*ds, s0, p, &r.t_gemm_iso, [&] {
+            return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
+        });
+        if (rc) return rc;
+        rc = time_phase(*ds, s0, p, &r.t_comm_iso, [&] {
+            return launch_coll(*ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, nullptr);
+        });
+        if (rc) return rc;
+        rc = time_phase(*ds, s0, p, &r.t_serial_meas, [&] {
+            int r1 = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
+            return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, nullptr);
+        });
+        if (rc) return rc;
+        if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
+        r.mode = mode;
+        r.sm_split = sm_split;
+        r.priority = priority;
+        rc = run_once(*ds, p, t, mode, sm_split, priority, &r);
+        r.status = rc;
+        if (rc) return rc;
+        fill_metrics(&r);
+        if (it >= warmup) per_rep[it - warmup] = r;
+    }
+    return C3_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+/*
+ * c3_api.h -- C ABI of libc3.so: concurrent computation and communication (C3)
+ * on one GB300 (sm_103a).
+ *
+ * The operation follows "Optimizing ML Concurrent Computation and
+ * Communication with GPU DMA Engines" (ConCCL, arXiv 2412.14335) as its review
+ * pages describe it: a GEMM runs at the same time as a bulk collective data
+ * movement (an all-gather or an all-to-all), and the quality of the overlap is
+ * measured against the ideal speedup (T_gemm + T_comm) / max(T_gemm, T_comm)
+ * taken from isolated runs (pith.science paper page: abstract, "The reading",
+ * referee report summary).  Four ways of running the pair are offered: the
+ * plain concurrent baseline, schedule prioritisation (collective first on a
+ * high-priority stream), SM partitioning (disjoint SM budgets) and copy-engine
+ * offload (the collective as DMA transfers, no SM kernel), with the option of
+ * taking SMs away from the GEMM while offloading (the paper's ConCCL_rp).
+ *
+ * The collective is emulated inside one device's memory: the buffers of
+ * `nranks` virtual ranks are separate device allocations of this GPU.
+ *
+ * Conventions for every entry point
+ *   - The caller owns all device memory and all streams passed in.  Device
+ *     pointers are plain CUDA device addresses of the current device; host
+ *     pointers are marked as such.  Nothing is freed or retained after return
+ *     except where stated.
+ *   - Streams are `cudaStream_t` values passed as `c3_stream` (void *); NULL
+ *     means the legacy default stream.
+ *   - The library owns a few internal objects per device, created on first use
+ *     with that device current and released by c3_shutdown(): two CUDA streams
+ *     (one at the highest priority), CUDA events, a 16 KiB device status block
+ *     (error word, %globaltimer stamps, per-CTA %smid residency records) and
+ *     the kernels' function attributes.
+ *   - Return value: C3_OK (0) or a negative c3_status.  On an argument error
+ *     nothing is launched.  C3_ECUDA carries the CUDA error text in
+ *     c3_last_error().  A device-side wait that gives up (a bounded spin on an
+ *     mbarrier, about two seconds) is reported as C3_ETIMEOUT by the next
+ *     synchronising call (c3_run, c3_time, c3_status_check).
+ *   - Not thread-safe: one host thread drives one device at a time.
+ */
+#ifndef C3_API_H
+#define C3_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *c3_stream; /* a cudaStream_t */
+
+typedef enum {
+    C3_OK = 0,
+    C3_EINVAL = -1,   /* bad argument: null pointer, negative size, unknown enum */
+    C3_EALIGN = -2,   /* pointer not 16-byte aligned, or size not a multiple of 16 bytes */
+    C3_ECUDA = -3,    /* a CUDA runtime/driver call failed; text in c3_last_error() */
+    C3_ETIMEOUT = -4, /* a bounded device wait gave up; results of that launch are void */
+    C3_EUNSUP = -5    /* valid request this build does not support (e.g. nranks != 8 on the CE 2-D path) */
+} c3_status;
+
+typedef enum { C3_ENGINE_SM = 0, C3_ENGINE_CE = 1 } c3_engine;
+typedef enum { C3_COLL_ALLGATHER = 0, C3_COLL_ALLTOALL = 1 } c3_coll;
+
+/* How the GEMM and the collective are run (see c3_run). */
+typedef enum {
+    C3_MODE_SERIAL_SM = 0,     /* GEMM, then the collective on SMs, one stream */
+    C3_MODE_CONCURRENT_SM = 1, /* GEMM || collective on SMs (baseline / prioritised / partitioned) */
+    C3_MODE_CONCURRENT_CE = 2, /* GEMM || collective on copy engines (ConCCL, ConCCL_rp) */
+    C3_MODE_SERIAL_CE = 3      /* GEMM, then the collective on copy engines, one stream */
+} c3_mode;
+
+/* SM copy kernel flavour.  VEC: 16-byte vector loads/stores, no shared memory,
+ * may share SMs with the GEMM.  BULK: cp.async.bulk global->shared->global
+ * through a shared-memory ring, one CTA per SM. */
+typedef enum { C3_SMK_AUTO = 0, C3_SMK_VEC = 1, C3_SMK_BULK = 2 } c3_sm_kernel;
+
+/* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
+typedef enum { C3_CLASS_G_LONG = 0, C3_CLASS_GC_EQUAL = 1, C3_CLASS_C_LONG = 2 } c3_class;
+
+typedef struct {
+    int device;           /* CUDA ordinal */
+    int sm_count;         /* streaming multiprocessors */
+    int l2_bytes;         /* L2 size */
+    int smem_per_sm;      /* shared memory per SM, bytes */
+    int smem_per_block;   /* opt-in maximum per CTA, bytes */
+    int cc_major, cc_minor;
+    int gemm_smem_bytes;  /* dynamic shared memory one GEMM CTA takes (largest tile) */
+    int comm_default_sms; /* SM budget of the SM collective when none is given */
+} c3_device_info;
+
+/* Library version and device facts (initialises the current device). */
+int c3_get_device_info(c3_device_info *out);
+/* Message for a status code (static string; never NULL). */
+const char *c3_strerror(int status);
+/* Detail of the most recent C3_ECUDA / C3_ETIMEOUT on this host thread. */
+const char *c3_last_error(void);
+/* Synchronises `s`, then reads and clears the device status word: C3_OK, or
+ * C3_ETIMEOUT if a kernel launched since the last check gave up a wait. */
+int c3_status_check(c3_stream s);
+/* Releases the library's per-device objects (streams, events, status block). */
+int c3_shutdown(void);
+/* Number of kernels this library has launched in this process (all devices),
+ * counted on the host at each successful launch.  Copy-engine transfers are
+ * not kernels and are not counted. */
+uint64_t c3_kernel_launches(void);
+
+/*
+ * GEMM:  C[m][n] = sum_k A[m][k] * B[n][k]            (the computation half of C3)
+ *   A  device, bf16, M x K row-major (K contiguous), 16-byte aligned
+ *   B  device, bf16, N x K row-major (the weight as an all-gather delivers it), 16-byte aligned
+ *   C  device, fp32, M x N row-major, written in full (no accumulation into C)
+ *   M, N >= 0 any value (ragged edges are masked); K >= 0 and K % 8 == 0
+ *      (the TMA row pitch must be a multiple of 16 bytes; else C3_EALIGN);
+ *      K == 0 writes zeros.  M*N == 0 launches nothing.
+ *   sm_budget  number of persistent CTAs, one per SM (0 = every SM); values
+ *      above the SM count are clamped.
+ * bf16 products are accumulated in fp32 on the tensor cores (tcgen05).
+ * Asynchronous on `s`.
+ */
+int c3_gemm(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+            int sm_budget, c3_stream s);
+
+/*
+ * All-gather over `nranks` virtual ranks of one device:
+ *   out[r * shard_bytes + i] = shards[r][i]   for r < nranks, i < shard_bytes
+ * (every rank's initial buffer concatenated in rank order: the check the
+ * pith.science verdict's skeptic critique asks for, "concrete_test").
+ *   shards  HOST array of nranks device pointers (read during the call only)
+ *   out     device, nranks * shard_bytes bytes; must not overlap any shard
+ *   shard_bytes  multiple of 16 (else C3_EALIGN); 0 launches nothing
+ *   nranks  1..64
+ *   engine  C3_ENGINE_SM: an SM copy kernel on `sm_budget` SMs (0 = default
+ *           budget); C3_ENGINE_CE: one cudaMemcpyAsync per shard (copy engine),
+ *           sm_budget ignored.
+ * Bit-exact byte copy.  Asynchronous on `s`.
+ */
+int c3_allgather(const void *const *shards, void *out, size_t shard_bytes, int nranks,
+                 int engine, int sm_budget, c3_stream s);
+
+/*
+ * All-to-all over an nranks x nranks grid of equal blocks:
+ *   out[(j * nranks + i) * block_bytes + b] = in[(i * nranks + j) * block_bytes + b]
+ * rank i's send buffer is in[i*nranks*block_bytes ...), its block j goes to
+ * receive slot i of rank j (the all-to-all the pages pair with the GEMM).
+ *   in, out  device, nranks^2 * block_bytes bytes each, not overlapping
+ *   block_bytes multiple of 16 (else C3_EALIGN); 0 launches nothing
+ *   nranks  1..8 (the SM kernel's segment table holds 64 blocks)
+ *   engine  as for c3_allgather (CE: one cudaMemcpyAsync per block)
+ * Bit-exact.  Asynchronous on `s`.
+ */
+int c3_alltoall(const void *in, void *out, size_t block_bytes, int nranks, int engine,
+                int sm_budget, c3_stream s);
+
+/* One C3 problem: a GEMM and one collective, both on caller-owned buffers. */
+typedef struct {
+    /* GEMM (as c3_gemm) */
+    const void *A;
+    const void *B;
+    float *C;
+    int64_t M, N, K;
+    /* collective */
+    int coll;                  /* c3_coll */
+    const void *const *shards; /* all-gather: HOST array of nranks device pointers */
+    const void *send;          /* all-to-all: send buffer */
+    void *recv;                /* output of the collective */
+    size_t unit_bytes;         /* shard bytes (all-gather) or block bytes (all-to-all) */
+    int nranks;
+    int comm_sms;              /* SM budget of the un-partitioned SM collective (0 = default) */
+    int sm_kernel;             /* c3_sm_kernel */
+    /* optional L2 flush between the phases of c3_time (caller-owned scratch,
+     * larger than L2; NULL = no flush) */
+    void *flush_buf;
+    size_t flush_bytes;
+    c3_stream stream;          /* runs fork from and join back to this stream */
+} c3_problem;
+
+/* Times in seconds. */
+typedef struct {
+    double t_gemm_iso;     /* GEMM alone, every SM                                  (c3_time) */
+    double t_comm_iso;     /* collective alone on the engine the mode uses           (c3_time) */
+    double t_serial;       /* t_gemm_iso + t_comm_iso: the serial time               (c3_time) */
+    double t_serial_meas;  /* GEMM then collective on one stream, measured           (c3_time) */
+    double t_conc;         /* fork to join of the requested mode                     (c3_run)  */
+    double t_ideal;        /* max(t_gemm_iso, t_comm_iso)                            (c3_time) */
+    double s_ideal;        /* t_serial / t_ideal                                     (c3_time) */
+    double s_real;         /* t_serial / t_conc                                      (c3_time) */
+    double pct_ideal_gain; /* (s_real - 1) / (s_ideal - 1): share of the ideal gain  (c3_time) */
+    double pct_ideal_ratio;/* s_real / s_ideal                                       (c3_time) */
+    double t_gemm_dev;     /* GEMM kernel window by %globaltimer (first CTA start to last CTA end) */
+    double t_comm_dev;     /* SM collective kernel window by %globaltimer (0 for CE) */
+    double t_gemm_ev;      /* fork to GEMM completion, CUDA events */
+    double t_comm_ev;      /* fork to collective completion, CUDA events */
+    int cls;               /* c3_class of (t_gemm_iso, t_comm_iso)                   (c3_time) */
+    int mode, sm_split, priority;
+    int gemm_ctas;         /* persistent GEMM CTAs launched */
+    int comm_ctas;         /* SM collective CTAs launched (0 for CE) */
+    int gemm_sms;          /* distinct SMs the GEMM CTAs ran on (%smid) */
+    int comm_sms;          /* distinct SMs the collective CTAs ran on */
+    int smid_overlap;      /* SMs on which a GEMM CTA and a collective CTA were resident at the
+                              same time, by their %globaltimer windows (0 = the partition held) */
+    int sms_shared_any;    /* SMs that ran CTAs of both kernels at any time during the run */
+    int status;            /* C3_OK or the run's device status */
+} c3_timing;
+
+/*
+ * One C3 execution of `p` in `mode`, synchronised, timed.
+ *   mode C3_MODE_CONCURRENT_SM:
+ *     sm_split == 0: baseline -- the GEMM on every SM and the collective with
+ *                    its default budget, free to share SMs;
+ *     sm_split  > 0: SM partitioning -- the collective on sm_split SMs it holds
+ *                    alone (its CTAs reserve enough shared memory that no GEMM
+ *                    CTA fits beside them) and the GEMM on the others.
+ *     priority == 1: schedule prioritisation -- the collective is launched
+ *                    first, on the library's highest-priority stream; 0: the
+ *                    GEMM is launched first and both streams have default
+ *                    priority.  (Pages: c3_sp, c3_rp and their combination.)
+ *   mode C3_MODE_CONCURRENT_CE: the collective as copy-engine transfers on its
+ *     own stream (ConCCL); sm_split > 0 removes that many SMs from the GEMM
+ *     (ConCCL_rp).  priority as above.
+ *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
+ * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
+ * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error
+ * (nothing launched) or the device status of the run.
+ */
+int c3_run(const c3_problem *p, int mode, int sm_split, int priority, c3_timing *out);
+
+/*
+ * The C3 timer: `warmup` untimed repetitions, then `reps` timed repetitions,
+ * each made of: GEMM alone (every SM), collective alone (the mode's engine,
+ * default budget), serial (GEMM then collective), and the requested mode.
+ * When p->flush_buf is set, L2 is flushed before each phase.  per_rep[r] (reps
+ * entries, host memory) receives every field, with the speedups of repetition
+ * r computed from that repetition's own isolated times.
+ */
+int c3_time(const c3_problem *p, int mode, int sm_split, int priority, int warmup, int reps,
+            c3_timing *per_rep);
+
+/* Writes `bytes` of zeros over `buf` (device) with an SM kernel: the L2 flush
+ * used between timed phases.  Asynchronous on `s`. */
+int c3_l2_flush(void *buf, size_t bytes, c3_stream s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* C3_API_H */

@@ -1,0 +1,130 @@
+"""Every C3 mode, run through c3_run / c3_time, followed by the check the
+pages' reviewers ask for: after each timed run, every output of the
+collective is compared byte for byte with the oracle and the GEMM with the
+oracle's tolerance (pith.science verdict, skeptic critique "concrete_test").
+Also: the partitioned modes really run on disjoint SMs (%smid maps), and the
+timer's derived fields obey their definitions."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from concurrent_communication_overlap_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+MODES = [  # (name, mode, sm_split, priority)
+    ("serial_sm", 0, 0, 0),
+    ("baseline", 1, 0, 0),
+    ("prioritised", 1, 0, 1),
+    ("partitioned16", 1, 16, 0),
+    ("partitioned32_prio", 1, 32, 1),
+    ("ce", 2, 0, 0),
+    ("ce_rp8", 2, 8, 0),
+    ("serial_ce", 3, 0, 0),
+]
+
+
+@pytest.fixture(scope="module")
+def c3():
+    from concurrent_communication_overlap_gb300 import c3 as mod
+    return mod
+
+
+class Setup:
+    def __init__(self, c3, wname):
+        w = I.WORKLOADS[wname]
+        self.w = w
+        A, B = I.gemm_operands(w)
+        self.C_ref, self.S_ref = oracle.gemm(A, B)
+        self.dA = torch.from_numpy(A.view(np.int16)).cuda()
+        self.dB = torch.from_numpy(B.view(np.int16)).cuda()
+        self.dC = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+        payload = I.coll_payload(w)
+        if w.coll == "allgather":
+            self.ref = oracle.allgather(payload)
+            self.dshards = [torch.from_numpy(s).cuda() for s in payload]
+            self.dsend = None
+            coll = c3.C3_COLL_ALLGATHER
+        else:
+            self.ref = oracle.alltoall(payload, w.nranks)
+            self.dshards = None
+            self.dsend = torch.from_numpy(payload).cuda()
+            coll = c3.C3_COLL_ALLTOALL
+        self.out = torch.empty(w.coll_bytes, dtype=torch.uint8, device="cuda")
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.p = c3.Problem(self.dA, self.dB, self.dC, w.M, w.N, w.K, coll, self.out, w.unit_bytes, w.nranks,
+                            shards=self.dshards, send=self.dsend, flush=self.flush)
+
+    def poison(self):
+        self.dC.fill_(float("nan"))
+        self.out.fill_(0xEE)
+        torch.cuda.synchronize()
+
+    def verify(self):
+        assert np.array_equal(self.out.cpu().numpy(), self.ref), "collective output differs from the oracle"
+        C = self.dC.cpu().numpy().astype(np.float64)
+        err = np.abs(C - self.C_ref)
+        assert not np.isnan(C).any()
+        assert (err <= TOL * self.S_ref).all(), float(np.max(err - TOL * self.S_ref))
+
+
+@pytest.fixture(scope="module", params=["tiny_ag", "tiny_a2a"])
+def setup(c3, request):
+    return Setup(c3, request.param)
+
+
+@pytest.mark.parametrize("name,mode,split,prio", MODES, ids=[m[0] for m in MODES])
+def test_mode_runs_and_outputs_are_exact(c3, setup, name, mode, split, prio):
+    setup.poison()
+    t = c3.c3_run(setup.p, mode, split, prio)
+    assert t["status"] == 0 and t["t_conc"] > 0
+    assert t["gemm_ctas"] >= 1
+    if mode in (2, 3):  # copy engines: no collective kernel ran
+        assert t["comm_ctas"] == 0 and t["comm_sms"] == 0
+    else:
+        assert t["comm_ctas"] >= 1 and t["comm_sms"] >= 1
+    setup.verify()
+
+
+@pytest.mark.parametrize("split", [8, 16, 32])
+def test_partitioned_runs_on_disjoint_sms(c3, setup, split):
+    info = c3.c3_get_device_info()
+    setup.poison()
+    t = c3.c3_run(setup.p, 1, split, 0)
+    # no SM ever held a GEMM CTA and a collective CTA at the same time
+    assert t["smid_overlap"] == 0, t
+    assert t["comm_sms"] <= split
+    assert t["gemm_ctas"] <= info["sm_count"] - split
+    setup.verify()
+
+
+def test_ce_with_gemm_cap_leaves_sms_free(c3, setup):
+    info = c3.c3_get_device_info()
+    t = c3.c3_run(setup.p, 2, 16, 0)
+    assert t["gemm_sms"] <= info["sm_count"] - 16
+    setup.verify()
+
+
+def test_timer_fields_follow_their_definitions(c3, setup):
+    reps = c3.c3_time(setup.p, 1, 0, 1, warmup=1, reps=3)
+    for r in reps:
+        assert r["t_gemm_iso"] > 0 and r["t_comm_iso"] > 0 and r["t_conc"] > 0
+        m = oracle.c3_metrics(r["t_gemm_iso"], r["t_comm_iso"], r["t_conc"])
+        assert r["t_serial"] == pytest.approx(m["t_serial"], rel=1e-12)
+        assert r["t_ideal"] == pytest.approx(m["t_ideal"], rel=1e-12)
+        assert r["s_ideal"] == pytest.approx(m["s_ideal"], rel=1e-12)
+        assert r["s_real"] == pytest.approx(m["s_real"], rel=1e-12)
+        assert r["pct_ideal_gain"] == pytest.approx(m["pct_ideal_gain"], rel=1e-9, abs=1e-12)
+        assert r["pct_ideal_ratio"] == pytest.approx(m["pct_ideal_ratio"], rel=1e-12)
+        assert r["class"] == m["class"]
+    setup.verify()
+
+
+def test_every_mode_under_c3_time_stays_exact(c3, setup):
+    for name, mode, split, prio in MODES:
+        setup.poison()
+        c3.c3_time(setup.p, mode, split, prio, warmup=0, reps=2)
+        setup.verify()

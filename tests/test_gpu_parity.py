@@ -1,0 +1,150 @@
+"""GPU parity: every kernel of libc3.so, called through the C ABI, against the
+CPU oracle on the same seeded inputs.
+
+Bars: collectives bit-exact; GEMM fp32 output within
+|gpu - oracle| <= 1e-4 * sum_k |a_ik b_kj| per element (the oracle computes
+the sum in fp64).  Sizes span several tiles with ragged tails; the full-size
+memory-bound workload is checked on sampled rows and entries."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from concurrent_communication_overlap_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def c3():
+    from concurrent_communication_overlap_gb300 import c3 as mod
+    return mod
+
+
+def dev_u16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def dev_bytes(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8)).cuda()
+
+
+def run_gemm(c3, A_bits, B_bits, sm_budget=0):
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    dA, dB = dev_u16(A_bits), dev_u16(B_bits)
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    c3.c3_gemm(dA, dB, dC, M, N, K, sm_budget)
+    c3.c3_status_check()
+    return dC.cpu().numpy()
+
+
+def assert_gemm_close(C_gpu, C_ref, S_ref):
+    err = np.abs(C_gpu.astype(np.float64) - C_ref)
+    bound = TOL * S_ref
+    bad = err > bound
+    assert not np.isnan(C_gpu).any(), "unwritten (NaN) outputs"
+    assert not bad.any(), f"{bad.sum()} elements out of tolerance; worst {np.max(err - bound)}"
+
+
+@pytest.mark.parametrize("M,N,K,budget", [
+    (512, 512, 512, 0),      # tiny workload's GEMM
+    (300, 200, 264, 0),      # ragged M, N, K tails (K not a multiple of the 64-wide stage)
+    (129, 33, 8, 0),         # one row / one column into the next tile, single short K step
+    (256, 203, 136, 0),      # N % 4 != 0: scalar store path
+    (512, 1024, 256, 4),     # few CTAs: wide tiles, many tiles per CTA, both accumulators reused
+    (384, 640, 192, 1),      # one CTA walks every tile
+    (1000, 1000, 512, 7),
+])
+def test_gemm_matches_oracle(c3, M, N, K, budget):
+    A = I.bf16_uniform(1000, (M, K), -1.0, 1.0)
+    B = I.bf16_uniform(1001, (N, K), -1.0, 1.0)
+    C = run_gemm(c3, A, B, budget)
+    C_ref, S_ref = oracle.gemm(A, B)
+    assert_gemm_close(C, C_ref, S_ref)
+
+
+def test_gemm_k_zero_writes_zeros(c3):
+    C = run_gemm(c3, np.zeros((70, 0), np.uint16), np.zeros((90, 0), np.uint16))
+    assert np.array_equal(C, np.zeros((70, 90), np.float32))
+
+
+def test_gemm_sm_budget_does_not_change_bits(c3):
+    A = I.bf16_normal(1000, (512, 512))
+    B = I.bf16_normal(1001, (768, 512), 0.0, 0.02)
+    ref = run_gemm(c3, A, B, 0)
+    for budget in (1, 5, 48, 10_000):
+        assert np.array_equal(run_gemm(c3, A, B, budget), ref)
+
+
+def test_gemm_special_values(c3):
+    # exact small-integer products and signed zeros survive the tensor-core path exactly
+    M, N, K = 128, 64, 64
+    a = ((np.arange(M * K) % 7) - 3).astype(np.float32).reshape(M, K)
+    b = ((np.arange(N * K) % 5) - 2).astype(np.float32).reshape(N, K)
+    C = run_gemm(c3, I.f32_to_bf16_bits(a), I.f32_to_bf16_bits(b))
+    assert np.array_equal(C, (a.astype(np.float64) @ b.T.astype(np.float64)).astype(np.float32))
+
+
+# ---------------------------------------------------------------- collectives
+
+AG_SIZES = [1 << 20, 16, 32 * 1024 + 16, 3 * 65536 + 4096 + 48]
+
+
+@pytest.mark.parametrize("shard_bytes", AG_SIZES)
+@pytest.mark.parametrize("engine,budget", [(0, 0), (0, 1), (0, 3), (1, 0)])
+def test_allgather_bit_exact(c3, shard_bytes, engine, budget):
+    shards = [I.random_bytes(1002 + r, shard_bytes) for r in range(8)]
+    ds = [dev_bytes(s) for s in shards]
+    out = torch.full((8 * shard_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    c3.c3_allgather(ds, out, shard_bytes, 8, engine=engine, sm_budget=budget)
+    c3.c3_status_check()
+    assert np.array_equal(out.cpu().numpy(), oracle.allgather(shards))
+
+
+@pytest.mark.parametrize("block", [128 * 1024, 16, 4096 + 32, 40 * 1024 + 16])
+@pytest.mark.parametrize("engine,budget", [(0, 0), (0, 2), (1, 0)])
+def test_alltoall_bit_exact(c3, block, engine, budget):
+    send = I.random_bytes(1002, 64 * block)
+    d_in = dev_bytes(send)
+    out = torch.full((64 * block,), 0x5A, dtype=torch.uint8, device="cuda")
+    c3.c3_alltoall(d_in, out, block, 8, engine=engine, sm_budget=budget)
+    c3.c3_status_check()
+    assert np.array_equal(out.cpu().numpy(), oracle.alltoall(send, 8))
+
+
+@pytest.mark.parametrize("nranks", [1, 2, 5])
+def test_collectives_other_rank_counts(c3, nranks):
+    sb = 4096 + 16
+    shards = [I.random_bytes(1002 + r, sb) for r in range(nranks)]
+    out = torch.zeros(nranks * sb, dtype=torch.uint8, device="cuda")
+    c3.c3_allgather([dev_bytes(s) for s in shards], out, sb, nranks)
+    send = I.random_bytes(7, nranks * nranks * 64)
+    o2 = torch.zeros(nranks * nranks * 64, dtype=torch.uint8, device="cuda")
+    c3.c3_alltoall(dev_bytes(send), o2, 64, nranks)
+    c3.c3_status_check()
+    assert np.array_equal(out.cpu().numpy(), oracle.allgather(shards))
+    assert np.array_equal(o2.cpu().numpy(), oracle.alltoall(send, nranks))
+
+
+def test_sm_kernel_flavours_bit_exact(c3):
+    # Both SM kernels (vector and cp.async.bulk ring) through the c3_run path.
+    w = I.WORKLOADS["tiny_ag"]
+    A, B = I.gemm_operands(w)
+    shards = I.coll_payload(w)
+    ref = oracle.allgather(shards)
+    C_ref, S_ref = oracle.gemm(A, B)
+    dA, dB = dev_u16(A), dev_u16(B)
+    ds = [dev_bytes(s) for s in shards]
+    for smk in (c3.C3_SMK_VEC, c3.C3_SMK_BULK):
+        for split in (0, 16):
+            dC = torch.full((w.M, w.N), float("nan"), device="cuda")
+            out = torch.zeros(w.coll_bytes, dtype=torch.uint8, device="cuda")
+            p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLGATHER, out, w.unit_bytes, 8,
+                           shards=ds, sm_kernel=smk)
+            t = c3.c3_run(p, c3.C3_MODE_CONCURRENT_SM, split, 0)
+            assert t["status"] == 0
+            assert np.array_equal(out.cpu().numpy(), ref), (smk, split)
+            assert_gemm_close(dC.cpu().numpy(), C_ref, S_ref)
