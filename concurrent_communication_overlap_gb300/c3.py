@@ -77,6 +77,7 @@ def _load():
         "c3_run": [ctypes.POINTER(C3Problem), _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_time": [ctypes.POINTER(C3Problem), _int, _int, _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_l2_flush": [_vp, _sz, _vp],
+        "c3_gemm_noalloc": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _int],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -91,7 +92,8 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
-            "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches")
+            "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
+            "c3_gemm_noalloc")
 
 
 def lib():
@@ -165,6 +167,13 @@ def c3_alltoall(inp, out, block_bytes, nranks, engine=C3_ENGINE_SM, sm_budget=0,
     rc = _lib.c3_alltoall(_ptr(inp), _ptr(out), int(block_bytes), int(nranks), int(engine), int(sm_budget),
                           _stream(stream))
     return _check(rc, "c3_alltoall") if check else rc
+
+
+def c3_gemm_noalloc(A, B, C, M, N, K, sm_budget=0, stream=None, sync_check=True, check=True):
+    """c3_gemm for callers that cannot allocate: scratch in a static device array."""
+    rc = _lib.c3_gemm_noalloc(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(sm_budget),
+                              _stream(stream), 1 if sync_check else 0)
+    return _check(rc, "c3_gemm_noalloc") if check else rc
 
 
 def c3_l2_flush(buf, nbytes, stream=None):

@@ -23,6 +23,7 @@
 #include "c3_device.cuh"
 #include "c3_internal.h"
 
+#include <cstdio>
 #include <mutex>
 
 namespace c3 {
@@ -363,3 +364,115 @@ int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, in
 }
 
 }  // namespace c3
+
+// ---------------------------------------------------------------- allocation-free GEMM entry point
+//
+// c3_gemm_noalloc: the GEMM for callers that must not allocate device memory
+// (see include/c3_api.h).  Its scratch -- the error word, the %globaltimer
+// window and the per-CTA residency records the kernel writes -- lives in the
+// file-scope array below instead of the library's cudaMalloc'd status block.
+// Host code cannot use the array's name as a device address, so the address
+// is looked up once per device with cudaGetSymbolAddress and cached.
+
+namespace c3 {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kStatusBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    int sm_count = 0;
+    DevStatus* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+static NoAllocDevice g_noalloc[64];
+static std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: the array's device address, the
+// SM count and the kernels' shared-memory attribute.  No allocation.
+static int noalloc_setup(NoAllocDevice** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return set_error(-5, "device ordinal out of range");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return set_cuda_error(e, "device attributes");
+        if (major != 10 || minor != 3) return set_error(-5, "libc3 is built for sm_103a (GB300) only");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+        d.scratch = static_cast<DevStatus*>(p);
+        int rc = gemm_init_device();
+        if (rc) return rc;
+        d.ready = true;
+    }
+    *out = &d;
+    return 0;
+}
+
+}  // namespace c3
+
+extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                               int sm_budget, void* stream, int check) {
+    using namespace c3;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M < 0 || N < 0 || K < 0 || sm_budget < 0) return set_error(-1, "negative size or sm_budget");
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return set_error(-5, "GEMM dimension above 2^31-1");
+    if (M == 0 || N == 0) return 0;
+    if (!C) return set_error(-1, "C is NULL");
+    if ((uintptr_t)C & 15u) return set_error(-2, "C must be 16-byte aligned");
+    if (K > 0) {
+        if (!A || !B) return set_error(-1, "A or B is NULL");
+        if (((uintptr_t)A | (uintptr_t)B) & 15u) return set_error(-2, "A and B must be 16-byte aligned");
+        if (K % 8) return set_error(-2, "K must be a multiple of 8 (16-byte TMA row pitch)");
+    }
+    NoAllocDevice* d = nullptr;
+    int rc = noalloc_setup(&d);
+    if (rc) return rc;
+    const int cap = (sm_budget <= 0 || sm_budget > d->sm_count) ? d->sm_count : sm_budget;
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * sizeof(float), s);
+        return e == cudaSuccess ? 0 : set_cuda_error(e, "cudaMemsetAsync");
+    }
+    const int bn = choose_bn(M, N, cap);
+    const int64_t num_m = (M + kBM - 1) / kBM;
+    const int64_t num_n = (N + bn - 1) / bn;
+    const int64_t tiles = num_m * num_n;
+    if (tiles > 0x7FFFFFFF) return set_error(-5, "GEMM has more than 2^31 tiles");
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    // The static block records at most kCtaRecs CTAs: refuse a launch that would need more.
+    if (grid > kCtaRecs)
+        return set_error(-5, "c3_gemm_noalloc: more than 256 CTAs would need more than its 16 KiB scratch");
+    CUtensorMap ma, mb;
+    if ((rc = make_map(&ma, A, M, K, kBM))) return rc;
+    if ((rc = make_map(&mb, B, N, K, bn))) return rc;
+    // The block keeps the previous call's contents: clear it on this stream first.
+    if ((rc = status_reset_launch(d->scratch, s))) return rc;
+    const int num_kb = (int)((K + kBK - 1) / kBK);
+    if (bn == 256)
+        gemm_bf16_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(
+            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, d->scratch);
+    else
+        gemm_bf16_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(
+            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, d->scratch);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "gemm kernel launch");
+    count_launch();
+    if (!check) return 0;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");
+    int err = 0, where = 0;
+    e = cudaMemcpy(&err, &d->scratch->error, sizeof err, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(&where, &d->scratch->where, sizeof where, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_cuda_error(e, "reading the scratch status word");
+    if (err) {
+        char buf[96];
+        std::snprintf(buf, sizeof buf, "device wait gave up (site %d)", where);
+        return set_error(err, buf);
+    }
+    return 0;
+}

@@ -234,6 +234,38 @@ int c3_run(const c3_problem *p, int mode, int sm_split, int priority, c3_timing 
 int c3_time(const c3_problem *p, int mode, int sm_split, int priority, int warmup, int reps,
             c3_timing *per_rep);
 
+/*
+ * The GEMM of c3_gemm for callers that cannot allocate device memory: code
+ * that runs where cudaMalloc is unavailable or forbidden (a host framework
+ * with its own fixed memory pool, a plugin called while a caller holds every
+ * byte of the device, real-time code that may not enter the allocator).  The
+ * pages have no counterpart of this entry point; it exists for those callers.
+ *
+ * Same arguments, result and ragged-edge handling as c3_gemm.  It allocates
+ * nothing: it does not touch the library's per-device state (no streams,
+ * events or status block are created), and calls no cudaMalloc, cudaFree or
+ * allocating library routine.  The scratch the GEMM kernel writes (error
+ * word, %globaltimer window, per-CTA SM records) is one file-scope device
+ * array of 16 KiB, present on every GPU that loads libc3.so until the process
+ * exits.  It records at most 256 CTAs: a launch that would need more (a GPU
+ * with more than 256 SMs and sm_budget 0 or above 256) is refused with
+ * C3_EUNSUP before anything is launched.
+ *
+ * The first call on each device does a one-time set-up with that device
+ * current (looks up the array's device address, reads the SM count, sets the
+ * kernels' shared-memory attribute); make that first call before any stream
+ * capture.  Each call clears the scratch on `s` before the GEMM, since the
+ * array keeps the previous call's contents.  All calls share the one array:
+ * calls whose executions overlap on the GPU (different streams, no ordering)
+ * race on it, and a caller must order them.
+ *   check  0: asynchronous on `s` (like c3_gemm); device wait timeouts are
+ *             then not reported.  Non-zero: synchronises `s` and returns
+ *             C3_ETIMEOUT if a bounded device wait of this GEMM gave up.
+ * K == 0 zero-fills C with cudaMemsetAsync.
+ */
+int c3_gemm_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                    int sm_budget, c3_stream s, int check);
+
 /* Writes `bytes` of zeros over `buf` (device) with an SM kernel: the L2 flush
  * used between timed phases.  Asynchronous on `s`. */
 int c3_l2_flush(void *buf, size_t bytes, c3_stream s);
