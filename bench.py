@@ -68,6 +68,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
+    ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
     return ap.parse_args(argv)
 
 
@@ -485,6 +486,8 @@ def main(argv=None):
     }
     line["clocks"] = clk.summary()
 
+    if not args.no_aux:
+        line["aux"] = aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info)
     if not args.no_e2e:
         line["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out, prob, modes,
                                   best, dev, stream, args)
@@ -498,6 +501,70 @@ def main(argv=None):
     if pg is not None:
         pg.destroy_process_group()
     return 0
+
+
+def _event_time(torch, stream, fn, reps, warm, flush=None):
+    """Mean device time (s) of fn() over reps launches on `stream`, L2 flushed
+    before each when `flush` is given (the flush is outside the timed interval)."""
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    return statistics.fmean(ts), ts
+
+
+def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
+    """Isolated kernel rates beside the C3 line: the GEMM on the compute-bound
+    shapes of the other workloads (TFLOP/s vs the dense bf16 peak), and the
+    collective's GB/s per SM budget for both SM kernels and the copy engines
+    (the pages' Figure 5b/c question: how many compute units a collective
+    needs)."""
+    res = {"gemm": {}, "copy_gbs_by_sms": {}}
+    flush_buf = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    do_flush = lambda: c3.c3_l2_flush(flush_buf, flush_buf.numel(), stream)  # noqa: E731
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    for (M, N, K) in [(8192, 8192, 8192), (8192, 28672, 8192)]:
+        A = (torch.randn((M, K), device=dev, generator=g)).to(torch.bfloat16)
+        B = (0.02 * torch.randn((N, K), device=dev, generator=g)).to(torch.bfloat16)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        t, _ = _event_time(torch, stream, lambda: c3.c3_gemm(A, B, C, M, N, K, 0, stream), 10, 3, do_flush)
+        tf = 2.0 * M * N * K / t / 1e12
+        res["gemm"][f"{M}x{N}x{K}"] = {"us": 1e6 * t, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                                        "plan": list(c3.c3_gemm_plan(M, N, K, 0))}
+        del A, B, C
+    if dshards is not None:
+        nbytes = 2 * w.coll_bytes
+        for kind, smk in (("vec", c3.C3_SMK_VEC), ("bulk", c3.C3_SMK_BULK)):
+            res["copy_gbs_by_sms"][kind] = {}
+            for k in (8, 16, 32, 64, 96, info["sm_count"]):
+                # c3_allgather has no flavour switch, so the collective runs through
+                # c3_run (serial mode) with an empty GEMM and the flavour in the record.
+                prob = c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLGATHER, out, w.unit_bytes, w.nranks,
+                                  shards=dshards, comm_sms=k, sm_kernel=smk, stream=stream)
+                tl = []
+                for _ in range(6):
+                    do_flush()
+                    tl.append(c3.c3_run(prob, c3.C3_MODE_SERIAL_SM, 0, 0)["t_conc"])
+                t = statistics.median(tl[1:])
+                res["copy_gbs_by_sms"][kind][str(k)] = nbytes / t / 1e9
+        tl = []
+        for _ in range(6):
+            do_flush()
+            tl.append(c3.c3_run(c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLGATHER, out, w.unit_bytes,
+                                           w.nranks, shards=dshards, stream=stream),
+                                c3.C3_MODE_SERIAL_CE, 0, 0)["t_conc"])
+        res["copy_gbs_by_sms"]["ce"] = nbytes / statistics.median(tl[1:]) / 1e9
+        res["copy_gbs_by_sms"]["peak_hbm_gbs"] = peaks["hbm_gbs"]
+    return res
 
 
 def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out, prob, modes, best, dev,

@@ -78,6 +78,7 @@ def _load():
         "c3_time": [ctypes.POINTER(C3Problem), _int, _int, _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_l2_flush": [_vp, _sz, _vp],
         "c3_gemm_noalloc": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _int],
+        "c3_gemm_plan": [_i64, _i64, _i64, _int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -93,7 +94,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
-            "c3_gemm_noalloc")
+            "c3_gemm_noalloc", "c3_gemm_plan")
 
 
 def lib():
@@ -174,6 +175,14 @@ def c3_gemm_noalloc(A, B, C, M, N, K, sm_budget=0, stream=None, sync_check=True,
     rc = _lib.c3_gemm_noalloc(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(sm_budget),
                               _stream(stream), 1 if sync_check else 0)
     return _check(rc, "c3_gemm_noalloc") if check else rc
+
+
+def c3_gemm_plan(M, N, K, sm_budget=0):
+    """(BN, 128-row sub-tiles per CTA, CTAs) that c3_gemm would launch."""
+    bn, ms, ctas = _int(), _int(), _int()
+    _check(_lib.c3_gemm_plan(int(M), int(N), int(K), int(sm_budget), ctypes.byref(bn), ctypes.byref(ms),
+                             ctypes.byref(ctas)), "c3_gemm_plan")
+    return bn.value, ms.value, ctas.value
 
 
 def c3_l2_flush(buf, nbytes, stream=None):

@@ -78,6 +78,7 @@ int set_error(int code, const char* what);
 // Kernels' host launchers.  Return 0 or a negative c3_status.
 int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
                 int sm_budget, cudaStream_t s, DevStatus* st, int* ctas_out);
+int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, int* grid);
 int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration
 int gemm_init_device();  // function attributes; once per device
 

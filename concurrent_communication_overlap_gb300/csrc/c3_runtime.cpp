@@ -443,6 +443,19 @@ int c3_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_
     return gemm_launch(A, B, C, M, N, K, sm_budget, static_cast<cudaStream_t>(s), ds->status, nullptr);
 }
 
+int c3_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_budget, int* bn, int* msub, int* ctas) {
+    if (!bn || !msub || !ctas) return set_error(C3_EINVAL, "output pointer is NULL");
+    if (M <= 0 || N <= 0 || K <= 0 || sm_budget < 0) return set_error(C3_EINVAL, "need M, N, K > 0, sm_budget >= 0");
+    int cap = sm_budget;
+    if (cap == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&cap, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return set_cuda_error(e, "SM count");
+    }
+    return gemm_describe(M, N, K, cap, bn, msub, ctas);
+}
+
 int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int nranks, int engine,
                  int sm_budget, c3_stream s) {
     if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");

@@ -28,21 +28,34 @@
 
 namespace c3 {
 
-constexpr int kBM = 128;
+constexpr int kBM = 128;          // rows of one MMA / one accumulator
 constexpr int kBK = 64;           // 64 bf16 = 128 bytes = one swizzle row
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
 constexpr int kGemmThreads = 192;
 constexpr int kGroupM = 16;
+constexpr int kSmemLimit = 232448;  // opt-in shared memory per CTA (227 KiB)
 
-template <int BN>
+// Tile of one CTA: MSUB x 128 rows (MSUB accumulators side by side in TMEM,
+// all fed by the same B tile) by BN columns.  Two accumulator sets when they
+// fit in TMEM's 512 columns, so the epilogue of one tile overlaps the main
+// loop of the next; one set otherwise.
+template <int BN, int MSUB>
 struct GemmCfg {
-    static constexpr int kStages = (BN == 256) ? 4 : 6;
-    static constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KiB
-    static constexpr uint32_t kBBytes = BN * kBK * 2;    // 32 or 16 KiB
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kTmemCols = 2 * BN;        // two accumulators
-    // ring + barriers + TMEM slot + abort flag, plus 1 KiB for 1024-byte alignment
-    static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+    static constexpr uint32_t kABytes = kBM * kBK * 2;           // 16 KiB per 128-row sub-tile
+    static constexpr uint32_t kBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = MSUB * kABytes + kBBytes;
+    static constexpr int kStagesFit = (kSmemLimit - 1024 - 512) / (int)kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr uint32_t kAccCols = MSUB * BN;              // fp32 columns of one accumulator set
+    static constexpr int kAccBufs = (2 * kAccCols <= 512) ? 2 : 1;
+    static constexpr uint32_t kUsedCols = kAccCols * kAccBufs;
+    static constexpr uint32_t kTmemCols = kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
+                                          : kUsedCols <= 256 ? 256 : 512;
+    // ring, then barriers / TMEM slot / abort flag (512 B), plus 1 KiB for alignment
+    static constexpr int kSmem = kStages * kStageBytes + 1024 + 512;
+    static_assert(kStages >= 2, "tile too large for the shared-memory ring");
+    static_assert(kUsedCols <= 512, "accumulators exceed TMEM");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128 is 16..256 step 16");
 };
 
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
@@ -74,25 +87,28 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
     nb = r / gm;
 }
 
-template <int BN>
+template <int BN, int MSUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      float* __restrict__ C, int M, int N, int num_m, int num_n, int num_kb,
                      DevStatus* st) {
-    using Cfg = GemmCfg<BN>;
+    using Cfg = GemmCfg<BN, MSUB>;
     constexpr int S = Cfg::kStages;
+    constexpr int NB = Cfg::kAccBufs;
+    constexpr int kRowsCta = kBM * MSUB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // ring: [A stage 0..S-1][B stage 0..S-1], then barriers
-    const uint32_t sA = base;
-    const uint32_t sB = base + S * Cfg::kABytes;
+    // ring: stage i = [A sub-tile 0 .. MSUB-1][B], then barriers
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * Cfg::kStageBytes);
-    // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem_full, [2S+2..2S+4) tmem_empty, [2S+4] drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    // bars[0..S) full, [S..2S) empty, [2S..2S+NB) tmem_full, [2S+NB..2S+2NB) tmem_empty, [2S+2NB] drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NB + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    auto stage_a = [&](int stage, int sub) { return base + (uint32_t)stage * Cfg::kStageBytes + (uint32_t)sub * Cfg::kABytes; };
+    auto stage_b = [&](int stage) { return base + (uint32_t)stage * Cfg::kStageBytes + MSUB * Cfg::kABytes; };
+    const int BAR_TFULL = 2 * S, BAR_TEMPTY = 2 * S + NB, BAR_DRAIN = 2 * S + 2 * NB;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -105,11 +121,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(bar(i), 1);
             mbar_init(bar(S + i), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(2 * S + b), 1);
-            mbar_init(bar(2 * S + 2 + b), 4 * 32);
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(bar(BAR_TFULL + b), 1);
+            mbar_init(bar(BAR_TEMPTY + b), 4 * 32);
         }
-        mbar_init(bar(2 * S + 4), 1);
+        mbar_init(bar(BAR_DRAIN), 1);
         fence_barrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -141,8 +157,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(bar(stage), Cfg::kStageBytes);
-                    tma_load_2d(sA + stage * Cfg::kABytes, &tmA, bar(stage), kb * kBK, mb * kBM, pol_a);
-                    tma_load_2d(sB + stage * Cfg::kBBytes, &tmB, bar(stage), kb * kBK, nb * BN, pol_b);
+#pragma unroll
+                    for (int sub = 0; sub < MSUB; ++sub)
+                        tma_load_2d(stage_a(stage, sub), &tmA, bar(stage), kb * kBK, mb * kRowsCta + sub * kBM, pol_a);
+                    tma_load_2d(stage_b(stage), &tmB, bar(stage), kb * kBK, nb * BN, pol_b);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -170,15 +188,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int local = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
-                const int buf = local & 1;
-                const uint32_t use = (uint32_t)(local >> 1);
-                if (!mbar_wait(bar(2 * S + 2 + buf), (use & 1u) ^ 1u, abort_flag)) {
+                const int buf = local % NB;
+                const uint32_t use = (uint32_t)(local / NB);
+                if (!mbar_wait(bar(BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag)) {
                     report_error(st, -4, kSiteGemmMma);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(buf * Cfg::kAccCols);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(bar(stage), phase, abort_flag)) {
                         report_error(st, -4, kSiteGemmMma);
@@ -186,13 +204,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = make_sdesc(sA + stage * Cfg::kABytes);
-                    const uint64_t bdesc = make_sdesc(sB + stage * Cfg::kBBytes);
+                    const uint64_t bdesc = make_sdesc(stage_b(stage));
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // advance 16 elements = 32 bytes inside the swizzled row
-                        tc_mma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int sub = 0; sub < MSUB; ++sub) {
+                            // advance 16 elements = 32 bytes inside the swizzled row
+                            const uint64_t adesc = make_sdesc(stage_a(stage, sub));
+                            tc_mma_bf16(d_tmem + (uint32_t)(sub * BN), adesc + (uint64_t)(2 * k),
+                                        bdesc + (uint64_t)(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     tc_commit(bar(S + stage));  // stage free once these MMAs have read it
                     if (++stage == S) {
@@ -200,12 +221,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         phase ^= 1u;
                     }
                 }
-                if (ok) tc_commit(bar(2 * S + buf));  // accumulator ready
+                if (ok) tc_commit(bar(BAR_TFULL + buf));  // accumulator set ready
             }
             // Whatever happened, make sure no MMA is still running before TMEM is freed.
-            tc_commit(bar(2 * S + 4));
+            tc_commit(bar(BAR_DRAIN));
             volatile int no_abort = 0;
-            if (!mbar_wait(bar(2 * S + 4), 0, &no_abort)) report_error(st, -4, kSiteGemmDrain);
+            if (!mbar_wait(bar(BAR_DRAIN), 0, &no_abort)) report_error(st, -4, kSiteGemmDrain);
         }
     } else {
         // ---------------- epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
@@ -213,11 +234,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const bool vec_ok = (N & 3) == 0;
         int local = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
-            const int buf = local & 1;
-            const uint32_t use = (uint32_t)(local >> 1);
+            const int buf = local % NB;
+            const uint32_t use = (uint32_t)(local / NB);
             // tcgen05.ld is warp-collective: the whole warp leaves together if
             // any lane's wait gave up.
-            const bool ready = mbar_wait(bar(2 * S + buf), use & 1u, abort_flag);
+            const bool ready = mbar_wait(bar(BAR_TFULL + buf), use & 1u, abort_flag);
             if (!__all_sync(0xffffffffu, ready)) {
                 report_error(st, -4, kSiteGemmEpilogue);
                 break;
@@ -225,31 +246,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             int mb, nb;
             tile_coords(t, num_m, num_n, mb, nb);
-            const int row = mb * kBM + q * 32 + lane;
-            float* crow = C + (size_t)row * (size_t)N;
-            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(taddr + (uint32_t)(c * 32), r);
-                tmem_ld_wait();
-                const int col0 = nb * BN + c * 32;
-                if (row < M) {
-                    if (vec_ok && col0 + 32 <= N) {
-                        float4* dst = reinterpret_cast<float4*>(crow + col0);
+            for (int sub = 0; sub < MSUB; ++sub) {
+                const int row = mb * kRowsCta + sub * kBM + q * 32 + lane;
+                float* crow = C + (size_t)row * (size_t)N;
+                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)(buf * Cfg::kAccCols + sub * BN);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    const int col0 = nb * BN + c * 32;
+                    if (row < M) {
+                        if (vec_ok && col0 + 32 <= N) {
+                            float4* dst = reinterpret_cast<float4*>(crow + col0);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                    } else {
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+                            for (int j = 0; j < 32; ++j)
+                                if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+                        }
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(2 * S + 2 + buf));
+            mbar_arrive(bar(BAR_TEMPTY + buf));
         }
     }
 
@@ -299,35 +324,105 @@ static int make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, 
     return 0;
 }
 
-int gemm_smem_bytes() { return GemmCfg<256>::kSmem > GemmCfg<128>::kSmem ? GemmCfg<256>::kSmem : GemmCfg<128>::kSmem; }
+// The tile configurations this build carries (BN x MSUB), in the order the
+// cost model breaks ties.
+struct TileCfg {
+    int bn, msub, stages, acc_bufs, smem;
+};
+#define C3_CFG(BN_, MS_) {BN_, MS_, GemmCfg<BN_, MS_>::kStages, GemmCfg<BN_, MS_>::kAccBufs, GemmCfg<BN_, MS_>::kSmem}
+static const TileCfg kCfgs[] = {C3_CFG(256, 1), C3_CFG(128, 1), C3_CFG(256, 2), C3_CFG(192, 2), C3_CFG(128, 2)};
+#undef C3_CFG
+constexpr int kNumCfgs = sizeof(kCfgs) / sizeof(kCfgs[0]);
+
+int gemm_smem_bytes() {
+    int m = 0;
+    for (const auto& c : kCfgs) m = c.smem > m ? c.smem : m;
+    return m;
+}
+
+template <int BN, int MS>
+static cudaError_t set_attr() {
+    return cudaFuncSetAttribute(gemm_bf16_kernel<BN, MS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                GemmCfg<BN, MS>::kSmem);
+}
 
 int gemm_init_device() {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmCfg<256>::kSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GemmCfg<128>::kSmem);
+    cudaError_t e = set_attr<256, 1>();
+    if (e == cudaSuccess) e = set_attr<128, 1>();
+    if (e == cudaSuccess) e = set_attr<256, 2>();
+    if (e == cudaSuccess) e = set_attr<192, 2>();
+    if (e == cudaSuccess) e = set_attr<128, 2>();
     if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(gemm)");
     return 0;
 }
 
-// Pick the tile width: the one whose busiest CTA has the least work, with a
-// fixed per-tile overhead (epilogue, pipeline fill) that favours wide tiles.
-static int choose_bn(int64_t M, int64_t N, int grid_cap) {
-    const int64_t num_m = (M + kBM - 1) / kBM;
-    int best_bn = 256;
-    double best = 1e300;
-    for (int bn : {256, 128}) {
-        const int64_t tiles = num_m * ((N + bn - 1) / bn);
-        const int64_t grid = tiles < grid_cap ? tiles : grid_cap;
-        const int64_t waves = (tiles + grid - 1) / grid;
-        const double cost = (double)waves * (bn + 32);
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_bn = bn;
+// Cost model for picking the tile configuration, in SM clock cycles of the
+// busiest CTA: per tile, the larger of the tensor-core time (4096 bf16 MACs
+// per cycle per SM) and the operand-load time (bytes into shared memory at an
+// assumed ~48 bytes per cycle per SM, the rate the single-tile kernel reached
+// on a latency-bound load), times the number of waves; with one accumulator
+// set the epilogue (fp32 tile out at ~64 bytes per cycle) does not overlap
+// and is added per tile.
+static int choose_cfg(int64_t M, int64_t N, int64_t K, int cap) {
+    int best = 0;
+    double best_cost = 1e300;
+    for (int i = 0; i < kNumCfgs; ++i) {
+        const TileCfg& c = kCfgs[i];
+        const int64_t rows = 128LL * c.msub;
+        const int64_t units = ((M + rows - 1) / rows) * ((N + c.bn - 1) / c.bn);
+        const int64_t grid = units < cap ? units : cap;
+        const int64_t waves = (units + grid - 1) / grid;
+        const double kk = (double)((K + 63) / 64 * 64);
+        const double mma = (double)rows * c.bn * kk / 4096.0;
+        const double load = (double)(rows + c.bn) * kk * 2.0 / 48.0;
+        const double epi = (double)rows * c.bn * 4.0 / 64.0;
+        const double per_tile = (mma > load ? mma : load) + (c.acc_bufs == 1 ? epi : 0.0);
+        const double cost = (double)waves * per_tile + epi;
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = i;
         }
     }
-    return best_bn;
+    return best;
+}
+
+static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, float* C, int64_t M, int64_t N,
+                      int64_t num_m, int64_t num_n, int num_kb, DevStatus* st, cudaStream_t s) {
+    const TileCfg& c = kCfgs[ci];
+#define C3_LAUNCH(BN_, MS_)                                                                                  \
+    gemm_bf16_kernel<BN_, MS_><<<grid, kGemmThreads, GemmCfg<BN_, MS_>::kSmem, s>>>(                           \
+        ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, st)
+    if (c.bn == 256 && c.msub == 1) C3_LAUNCH(256, 1);
+    else if (c.bn == 128 && c.msub == 1) C3_LAUNCH(128, 1);
+    else if (c.bn == 256 && c.msub == 2) C3_LAUNCH(256, 2);
+    else if (c.bn == 192 && c.msub == 2) C3_LAUNCH(192, 2);
+    else C3_LAUNCH(128, 2);
+#undef C3_LAUNCH
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "gemm kernel launch");
+    count_launch();
+    return 0;
+}
+
+// Plans one GEMM: configuration, grid, tensor maps.
+struct GemmPlan {
+    int ci, grid, num_kb;
+    int64_t num_m, num_n;
+    CUtensorMap ma, mb;
+};
+
+static int plan_gemm(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int cap, GemmPlan* p) {
+    p->ci = choose_cfg(M, N, K, cap);
+    const TileCfg& c = kCfgs[p->ci];
+    p->num_m = (M + 128LL * c.msub - 1) / (128LL * c.msub);
+    p->num_n = (N + c.bn - 1) / c.bn;
+    const int64_t tiles = p->num_m * p->num_n;
+    if (tiles > 0x7FFFFFFF) return set_error(-5, "GEMM has more than 2^31 tiles");
+    p->grid = (int)(tiles < cap ? tiles : cap);
+    p->num_kb = (int)((K + kBK - 1) / kBK);
+    int rc = make_map(&p->ma, A, M, K, kBM);
+    if (rc) return rc;
+    return make_map(&p->mb, B, N, K, c.bn);
 }
 
 int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
@@ -337,29 +432,23 @@ int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, in
     if (K == 0) return zero_fill_launch(C, (size_t)M * (size_t)N * sizeof(float), s);
     DeviceState* ds = device_state();
     if (!ds) return -3;
-    int cap = (sm_budget <= 0 || sm_budget > ds->sm_count) ? ds->sm_count : sm_budget;
-    const int bn = choose_bn(M, N, cap);
-    const int64_t num_m = (M + kBM - 1) / kBM;
-    const int64_t num_n = (N + bn - 1) / bn;
-    const int64_t tiles = num_m * num_n;
-    if (tiles > 0x7FFFFFFF) return set_error(-5, "GEMM has more than 2^31 tiles");
-    const int grid = (int)(tiles < cap ? tiles : cap);
-    const int num_kb = (int)((K + kBK - 1) / kBK);
-    CUtensorMap ma, mb;
-    int rc = make_map(&ma, A, M, K, kBM);
+    const int cap = (sm_budget <= 0 || sm_budget > ds->sm_count) ? ds->sm_count : sm_budget;
+    GemmPlan p;
+    int rc = plan_gemm(A, B, M, N, K, cap, &p);
     if (rc) return rc;
-    rc = make_map(&mb, B, N, K, bn);
+    rc = launch_cfg(p.ci, p.grid, p.ma, p.mb, C, M, N, p.num_m, p.num_n, p.num_kb, st, s);
     if (rc) return rc;
-    if (bn == 256)
-        gemm_bf16_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(
-            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, st);
-    else
-        gemm_bf16_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(
-            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, st);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_cuda_error(e, "gemm kernel launch");
-    count_launch();
-    if (ctas_out) *ctas_out = grid;
+    if (ctas_out) *ctas_out = p.grid;
+    return 0;
+}
+
+int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, int* grid) {
+    const int ci = choose_cfg(M, N, K, cap);
+    const TileCfg& c = kCfgs[ci];
+    const int64_t tiles = ((M + 128LL * c.msub - 1) / (128LL * c.msub)) * ((N + c.bn - 1) / c.bn);
+    *bn = c.bn;
+    *msub = c.msub;
+    *grid = (int)(tiles < cap ? tiles : cap);
     return 0;
 }
 
@@ -438,30 +527,17 @@ extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M
         cudaError_t e = cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * sizeof(float), s);
         return e == cudaSuccess ? 0 : set_cuda_error(e, "cudaMemsetAsync");
     }
-    const int bn = choose_bn(M, N, cap);
-    const int64_t num_m = (M + kBM - 1) / kBM;
-    const int64_t num_n = (N + bn - 1) / bn;
-    const int64_t tiles = num_m * num_n;
-    if (tiles > 0x7FFFFFFF) return set_error(-5, "GEMM has more than 2^31 tiles");
-    const int grid = (int)(tiles < cap ? tiles : cap);
+    GemmPlan plan;
+    if ((rc = plan_gemm(A, B, M, N, K, cap, &plan))) return rc;
     // The static block records at most kCtaRecs CTAs: refuse a launch that would need more.
-    if (grid > kCtaRecs)
+    if (plan.grid > kCtaRecs)
         return set_error(-5, "c3_gemm_noalloc: more than 256 CTAs would need more than its 16 KiB scratch");
-    CUtensorMap ma, mb;
-    if ((rc = make_map(&ma, A, M, K, kBM))) return rc;
-    if ((rc = make_map(&mb, B, N, K, bn))) return rc;
     // The block keeps the previous call's contents: clear it on this stream first.
     if ((rc = status_reset_launch(d->scratch, s))) return rc;
-    const int num_kb = (int)((K + kBK - 1) / kBK);
-    if (bn == 256)
-        gemm_bf16_kernel<256><<<grid, kGemmThreads, GemmCfg<256>::kSmem, s>>>(
-            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, d->scratch);
-    else
-        gemm_bf16_kernel<128><<<grid, kGemmThreads, GemmCfg<128>::kSmem, s>>>(
-            ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, d->scratch);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return set_cuda_error(e, "gemm kernel launch");
-    count_launch();
+    if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, C, M, N, plan.num_m, plan.num_n, plan.num_kb,
+                         d->scratch, s)))
+        return rc;
+    cudaError_t e;
     if (!check) return 0;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");

@@ -120,6 +120,14 @@ int c3_gemm(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_
             int sm_budget, c3_stream s);
 
 /*
+ * The launch c3_gemm would make for this shape and budget, without launching:
+ * the tile width BN, the number of 128-row sub-tiles per CTA (1 or 2) and the
+ * number of persistent CTAs.  Host only (reads the SM count of the current
+ * device when sm_budget is 0).
+ */
+int c3_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_budget, int *bn, int *msub, int *ctas);
+
+/*
  * All-gather over `nranks` virtual ranks of one device:
  *   out[r * shard_bytes + i] = shards[r][i]   for r < nranks, i < shard_bytes
  * (every rank's initial buffer concatenated in rank order: the check the

@@ -49,21 +49,45 @@ def assert_gemm_close(C_gpu, C_ref, S_ref):
     assert not bad.any(), f"{bad.sum()} elements out of tolerance; worst {np.max(err - bound)}"
 
 
-@pytest.mark.parametrize("M,N,K,budget", [
-    (512, 512, 512, 0),      # tiny workload's GEMM
-    (300, 200, 264, 0),      # ragged M, N, K tails (K not a multiple of the 64-wide stage)
-    (129, 33, 8, 0),         # one row / one column into the next tile, single short K step
-    (256, 203, 136, 0),      # N % 4 != 0: scalar store path
-    (512, 1024, 256, 4),     # few CTAs: wide tiles, many tiles per CTA, both accumulators reused
-    (384, 640, 192, 1),      # one CTA walks every tile
-    (1000, 1000, 512, 7),
+@pytest.mark.parametrize("M,N,K,budget,plan", [
+    (512, 512, 512, 0, (128, 1)),      # tiny workload's GEMM
+    (300, 200, 264, 0, (128, 1)),      # ragged M, N, K tails (K not a multiple of the 64-wide stage)
+    (129, 33, 8, 0, None),             # one row / one column into the next tile, single short K step
+    (256, 203, 136, 0, None),          # N % 4 != 0: scalar store path
+    (384, 640, 192, 1, None),          # one CTA walks every tile
+    (1000, 1000, 512, 7, None),
+    # every tile configuration, ragged in M and N, at least 3 tiles per CTA:
+    (300, 500, 200, 2, (256, 1)),
+    (300, 500, 200, 4, (128, 1)),
+    (400, 700, 520, 2, (256, 2)),      # two 128-row sub-tiles per CTA, one accumulator set
+    (400, 1100, 200, 2, (128, 2)),     # two sub-tiles, two accumulator sets
+    (400, 1100, 520, 4, (192, 2)),     # the memory-bound workload's configuration
 ])
-def test_gemm_matches_oracle(c3, M, N, K, budget):
+def test_gemm_matches_oracle(c3, M, N, K, budget, plan):
+    if plan is not None:
+        assert c3.c3_gemm_plan(M, N, K, budget)[:2] == plan
     A = I.bf16_uniform(1000, (M, K), -1.0, 1.0)
     B = I.bf16_uniform(1001, (N, K), -1.0, 1.0)
     C = run_gemm(c3, A, B, budget)
     C_ref, S_ref = oracle.gemm(A, B)
     assert_gemm_close(C, C_ref, S_ref)
+
+
+def test_gemm_full_size_memory_bound_sampled(c3):
+    # The bench workload in the bench's launch configuration: 256 x 28672 x 8192,
+    # N(0,1) activations, N(0,0.02) weights, every SM.  Checked on 6 full rows
+    # (every column, every tile) and 512 random entries against the oracle.
+    w = I.WORKLOADS["mem_ag"]
+    assert c3.c3_gemm_plan(w.M, w.N, w.K, 0)[:2] == (192, 2)
+    A, B = I.gemm_operands(w)
+    C = run_gemm(c3, A, B, 0)
+    rows = np.array([0, 1, 127, 128, 200, 255])
+    C_ref, S_ref = oracle.gemm(A[rows], B)
+    assert_gemm_close(C[rows], C_ref, S_ref)
+    rng = np.random.default_rng(5)
+    mi, ni = rng.integers(0, w.M, 512), rng.integers(0, w.N, 512)
+    c_ref, s_ref = oracle.gemm_entries(A, B, mi, ni)
+    assert_gemm_close(C[mi, ni], c_ref, s_ref)
 
 
 def test_gemm_k_zero_writes_zeros(c3):
