@@ -115,10 +115,11 @@ DeviceState* device_state() {
 }
 
 static int default_comm_sms(const DeviceState& ds) {
-    // About a fifth of the SMs: the share the pages' library gives its
-    // all-gather kernel by default (64 of 304 compute units, Figure 5 caption).
-    int k = (ds.sm_count * 64 + 303) / 304;
-    return k < 1 ? 1 : k;
+    // One vector-copy CTA per SM: the budget at which the SM collective is
+    // fastest alone on GB300 (a fifth of the SMs, the share the pages' library
+    // gives its all-gather by default -- 64 of 304 compute units, Figure 5
+    // caption -- moves less than half as many bytes per second here).
+    return ds.sm_count;
 }
 
 // Shared memory a partitioned collective CTA reserves so that neither a GEMM
