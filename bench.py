@@ -69,6 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
     ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
+    ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
+                    help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
     return ap.parse_args(argv)
 
 
@@ -344,6 +346,55 @@ def run_reference(args, world, rank, pg):
     return 0
 
 
+def run_sweep(args, c3, torch, np, I, dev, info):
+    """The pages' size sweep: an 8192^3 GEMM against collectives of 1 MiB to
+    1 GiB total (x2 steps), every mode of --modes (default: baseline,
+    prioritised, partitioned_32, ce), one JSON line per size."""
+    names = args.modes.split(",") if args.modes else ["baseline", "prioritised", "partitioned_32", "ce"]
+    modes = [m for m in MODES if m[0] in names]
+    ws = I.sweep_workloads(args.sweep)
+    w0 = ws[0]
+    A_h, B_h = I.gemm_operands(w0)
+    dA = torch.from_numpy(A_h.view(np.int16)).to(dev)
+    dB = torch.from_numpy(B_h.view(np.int16)).to(dev)
+    dC = torch.empty((w0.M, w0.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for w in ws:
+        payload = I.coll_payload(w)
+        if w.coll == "allgather":
+            dsh = [torch.from_numpy(x).to(dev) for x in payload]
+            dsend, cid, ref = None, c3.C3_COLL_ALLGATHER, np.concatenate(payload)
+        else:
+            import oracle
+            dsh, dsend, cid = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
+            ref = oracle.alltoall(payload, w.nranks)
+        out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
+        prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, cid, out, w.unit_bytes, w.nranks, shards=dsh, send=dsend,
+                          flush=flush, stream=stream)
+        per = {m[0]: [] for m in modes}
+        for it in range(args.warmup + args.steps):
+            for name, mode, split, prio in modes:
+                r = c3.c3_time(prob, mode, split, prio, warmup=0, reps=1)
+                if it >= args.warmup:
+                    per[name].extend(r)
+        exact = bool(np.array_equal(out.cpu().numpy(), ref))
+        res = {}
+        for name, recs in per.items():
+            tg = statistics.median(r["t_gemm_iso"] for r in recs)
+            tc = statistics.median(r["t_comm_iso"] for r in recs)
+            tconc = statistics.median(r["t_conc"] for r in recs)
+            m = pct_gain(tg, tc, tconc)
+            res[name] = {"t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc, "t_conc_us": 1e6 * tconc,
+                         "s_ideal": m["s_ideal"], "s_real": m["s_real"], "pct_ideal_gain": m["pct_ideal_gain"],
+                         "pct_ideal_ratio": m["pct_ideal_ratio"], "class": recs[0]["class"]}
+        best = max(res, key=lambda k: res[k]["pct_ideal_gain"] if res[k]["s_ideal"] > 1.0 else -1e9)
+        print(json.dumps({"sweep": args.sweep, "workload": w.name, "coll_bytes": w.coll_bytes, "steps": args.steps,
+                          "collective_bit_exact": exact, "best_mode": best, "modes": res}), flush=True)
+        del out, dsh, dsend, prob
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local, pg = dist_init(args)
@@ -360,8 +411,10 @@ def main(argv=None):
         raise SystemExit("bench.py needs a CUDA device (GB300); there is no CPU path")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = I.WORKLOADS[args.workload]
     info = c3.c3_get_device_info()
+    if args.sweep:
+        return run_sweep(args, c3, torch, np, I, dev, info)
+    w = I.WORKLOADS[args.workload]
     modes = MODES if not args.modes else [m for m in MODES if m[0] in args.modes.split(",")]
 
     # ---- inputs (host-generated, seeded), resident in HBM before timing

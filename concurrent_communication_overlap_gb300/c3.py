@@ -78,6 +78,7 @@ def _load():
         "c3_time": [ctypes.POINTER(C3Problem), _int, _int, _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_l2_flush": [_vp, _sz, _vp],
         "c3_gemm_noalloc": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _int],
+        "c3_selftest_wait": [ctypes.c_uint64, _int, _vp],
         "c3_gemm_plan": [_i64, _i64, _i64, _int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)],
     }
     for name, args in sig.items():
@@ -94,7 +95,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
-            "c3_gemm_noalloc", "c3_gemm_plan")
+            "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait")
 
 
 def lib():
@@ -183,6 +184,11 @@ def c3_gemm_plan(M, N, K, sm_budget=0):
     _check(_lib.c3_gemm_plan(int(M), int(N), int(K), int(sm_budget), ctypes.byref(bn), ctypes.byref(ms),
                              ctypes.byref(ctas)), "c3_gemm_plan")
     return bn.value, ms.value, ctas.value
+
+
+def c3_selftest_wait(limit_ns, arrive, stream=None):
+    """Status of a bounded device wait that succeeds (arrive=1) or runs out (arrive=0)."""
+    return int(_lib.c3_selftest_wait(int(limit_ns), int(arrive), _stream(stream)))
 
 
 def c3_l2_flush(buf, nbytes, stream=None):

@@ -25,6 +25,7 @@ enum WaitSite : int {
     kSiteGemmDrain = 4,
     kSiteBulkLoad = 5,
     kSiteBulkDrain = 6,
+    kSiteSelfTest = 7,
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -117,14 +118,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase of parity `parity` has completed.  Gives up (and
 // raises *abort) after kWaitLimitNs, or returns false at once when another
 // role of the CTA has already raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }

@@ -90,6 +90,7 @@ int bulk_copy_smem_bytes();
 int copy_ce_launch(const SegTable& t, cudaStream_t s);
 
 int status_reset_launch(DevStatus* st, cudaStream_t s);
+int selftest_wait_launch(DevStatus* st, unsigned long long limit_ns, int arrive, cudaStream_t s);
 int zero_fill_launch(void* buf, size_t bytes, cudaStream_t s);
 
 }  // namespace c3

@@ -483,6 +483,25 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
+int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s) {
+    if (limit_ns == 0 || limit_ns > 5000000000ull) return set_error(C3_EINVAL, "limit_ns must be 1 ns .. 5 s");
+    if (arrive != 0 && arrive != 1) return set_error(C3_EINVAL, "arrive must be 0 or 1");
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(s);
+    int rc = status_reset_launch(ds->status, st);
+    if (rc) return rc;
+    if ((rc = selftest_wait_launch(ds->status, limit_ns, arrive, st))) return rc;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");
+    const int status = read_status(*ds, nullptr);
+    // leave a clean status block behind, so later checks do not see this test
+    if ((rc = status_reset_launch(ds->status, st))) return rc;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");
+    return status;
+}
+
 int c3_l2_flush(void* buf, size_t bytes, c3_stream s) {
     if (!buf && bytes) return set_error(C3_EINVAL, "buf is NULL");
     if (!aligned16(buf)) return set_error(C3_EALIGN, "buf must be 16-byte aligned");

@@ -44,6 +44,31 @@ __global__ void zero_fill_kernel(uint8_t* buf, size_t bytes) {
         for (size_t b = nvec << 4; b < bytes; ++b) buf[b] = 0;
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier phase.  With
+// `arrive` the phase completes first and the wait succeeds; without it nothing
+// ever completes the phase and the wait must give up after limit_ns and
+// report C3_ETIMEOUT.  Nothing else runs in the kernel; no memory is touched
+// but the status block.
+__global__ void wait_selftest_kernel(DevStatus* st, unsigned long long limit_ns, int arrive) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_barrier_init();
+    if (arrive) mbar_arrive(b);
+    if (!mbar_wait(b, 0, &abort_flag, limit_ns)) report_error(st, -4, kSiteSelfTest);
+}
+
+int selftest_wait_launch(DevStatus* st, unsigned long long limit_ns, int arrive, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(st, limit_ns, arrive);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "self-test launch");
+    count_launch();
+    return 0;
+}
+
 int status_reset_launch(DevStatus* st, cudaStream_t s) {
     status_reset_kernel<<<1, kCtaRecs, 0, s>>>(st);
     cudaError_t e = cudaGetLastError();

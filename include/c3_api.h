@@ -274,6 +274,18 @@ int c3_time(const c3_problem *p, int mode, int sm_split, int priority, int warmu
 int c3_gemm_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
                     int sm_budget, c3_stream s, int check);
 
+/*
+ * Self-test of the library's failure detection: launches one kernel whose
+ * single thread waits on an mbarrier phase with the same bounded wait the
+ * GEMM and the bulk copy use, limited to `limit_ns` (1 ns .. 5 s, else
+ * C3_EINVAL).  arrive = 1: the phase is completed first, the wait succeeds,
+ * C3_OK.  arrive = 0: nothing completes the phase, the wait gives up after
+ * the limit and the call returns C3_ETIMEOUT -- with the CUDA context intact.
+ * Synchronises `s`.  The pages have no counterpart (failure handling is this
+ * library's own).
+ */
+int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s);
+
 /* Writes `bytes` of zeros over `buf` (device) with an SM kernel: the L2 flush
  * used between timed phases.  Asynchronous on `s`. */
 int c3_l2_flush(void *buf, size_t bytes, c3_stream s);

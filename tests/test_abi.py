@@ -98,6 +98,9 @@ def test_argument_errors_before_any_cuda_call(c3):
     assert c3.c3_gemm_noalloc(0x1000, 0x1000, 0x1000, -1, 4, 8, check=False) == c3.C3_EINVAL
     assert c3.c3_gemm_noalloc(0x1000, 0x1000, 0x1000, 4, 4, 12, check=False) == c3.C3_EALIGN
     assert c3.c3_gemm_noalloc(None, None, None, 4, 0, 8, check=False) == c3.C3_OK
+    assert c3.c3_selftest_wait(0, 0) == c3.C3_EINVAL
+    assert c3.c3_selftest_wait(6_000_000_000, 0) == c3.C3_EINVAL
+    assert c3.c3_selftest_wait(1000, 2) == c3.C3_EINVAL
     assert c3.lib().c3_l2_flush(0x1001, 64, None) == c3.C3_EALIGN
     assert c3.lib().c3_l2_flush(None, 64, None) == c3.C3_EINVAL
 
