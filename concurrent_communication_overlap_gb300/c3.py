@@ -20,6 +20,7 @@ C3_ENGINE_SM, C3_ENGINE_CE = 0, 1
 C3_COLL_ALLGATHER, C3_COLL_ALLTOALL = 0, 1
 C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_CE = 0, 1, 2, 3
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
+C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
 CLASS_NAMES = {0: "G-long", 1: "GC-equal", 2: "C-long"}
 
 _i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -34,7 +35,7 @@ class C3DeviceInfo(ctypes.Structure):
 class C3Problem(ctypes.Structure):
     _fields_ = [("A", _vp), ("B", _vp), ("C", _vp), ("M", _i64), ("N", _i64), ("K", _i64),
                 ("coll", _int), ("shards", ctypes.POINTER(_vp)), ("send", _vp), ("recv", _vp),
-                ("unit_bytes", _sz), ("nranks", _int), ("comm_sms", _int), ("sm_kernel", _int),
+                ("unit_bytes", _sz), ("nranks", _int), ("comm_sms", _int), ("sm_kernel", _int), ("coll_l2", _int),
                 ("flush_buf", _vp), ("flush_bytes", _sz), ("stream", _vp)]
 
 
@@ -199,14 +200,14 @@ class Problem:
     """Owns the ctypes problem record and keeps the host shard-pointer array alive."""
 
     def __init__(self, A, B, C, M, N, K, coll, recv, unit_bytes, nranks=8, shards=None, send=None,
-                 comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None):
+                 comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None, coll_l2=C3_L2_NORMAL):
         self._shard_arr = None
         if shards is not None:
             self._shard_arr = (_vp * len(shards))(*[_ptr(s) for s in shards])
         fb, fn = (None, 0) if flush is None else (_ptr(flush), flush.numel() * flush.element_size())
         self.rec = C3Problem(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(coll),
                              self._shard_arr, _ptr(send), _ptr(recv), int(unit_bytes), int(nranks),
-                             int(comm_sms), int(sm_kernel), fb, fn, _stream(stream))
+                             int(comm_sms), int(sm_kernel), int(coll_l2), fb, fn, _stream(stream))
 
 
 def c3_run(problem: Problem, mode, sm_split=0, priority=0, check=True):

@@ -82,7 +82,7 @@ int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, 
 int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration
 int gemm_init_device();  // function attributes; once per device
 
-int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, cudaStream_t s,
+int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, int l2_stream, cudaStream_t s,
                    DevStatus* st, int* ctas_out);
 int copy_init_device(int max_reserve);
 int bulk_copy_smem_bytes();

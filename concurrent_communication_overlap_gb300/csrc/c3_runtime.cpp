@@ -192,7 +192,7 @@ static int build_alltoall(const void* in, void* out, size_t block_bytes, int nra
 
 // One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
 // the CTAs keep their SMs to themselves (partitioning).
-static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int budget,
+static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int l2_stream, int budget,
                        bool exclusive, cudaStream_t s, int* ctas) {
     if (ctas) *ctas = 0;
     if (engine == C3_ENGINE_CE) return copy_ce_launch(t, s);
@@ -202,7 +202,7 @@ static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_ke
                   : sm_kernel == C3_SMK_BULK ? kSmkBulk
                   : (exclusive ? kSmkBulk : kSmkVec);
     int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-    return copy_sm_launch(t, k, flavour, reserve, s, ds.status, ctas);
+    return copy_sm_launch(t, k, flavour, reserve, l2_stream, s, ds.status, ctas);
 }
 
 static int wait_event(cudaEvent_t ev, double limit_s) {
@@ -280,6 +280,7 @@ static int check_problem(const c3_problem* p, SegTable* t) {
         return set_error(C3_EINVAL, "unknown collective");
     if (rc) return rc;
     if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
+    if (p->coll_l2 != C3_L2_NORMAL && p->coll_l2 != C3_L2_EVICT_FIRST) return set_error(C3_EINVAL, "bad coll_l2");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
     if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
     const size_t cb = t->seg_bytes * (size_t)t->nseg;
@@ -305,7 +306,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int
         rc = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds.status, &gctas);
         if (rc) return rc;
         if ((e = cudaEventRecord(ev_g, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
-        rc = launch_coll(ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, &cctas);
+        rc = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, &cctas);
         if (rc) return rc;
         if ((e = cudaEventRecord(ev_c, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     } else {
@@ -319,7 +320,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
         auto go_gemm = [&] { return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, gemm_budget, sg, ds.status, &gctas); };
-        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, comm_budget, part, sc, &cctas); };
+        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, comm_budget, part, sc, &cctas); };
         if (priority) {
             if ((rc = go_comm())) return rc;
             if ((rc = go_gemm())) return rc;
@@ -467,7 +468,7 @@ int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int n
     if (shard_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int engine, int sm_budget,
@@ -480,7 +481,7 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     if (block_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s) {
@@ -548,12 +549,12 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
         });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_comm_iso, [&] {
-            return launch_coll(*ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, nullptr);
+            return launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_serial_meas, [&] {
             int r1 = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
-            return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->comm_sms, false, s0, nullptr);
+            return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
         if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;

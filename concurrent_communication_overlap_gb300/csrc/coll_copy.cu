@@ -18,6 +18,9 @@
 //           with cp.async.bulk through a 6-deep shared-memory ring (192 KiB in
 //           flight per SM, no register staging).  One CTA per SM by its
 //           shared-memory footprint.
+// Each flavour has a streaming variant whose loads and stores carry an L2
+// evict-first policy (and skip L1), the software counterpart of the pages'
+// observation that DMA transfers bypass the caches.
 #include "c3_device.cuh"
 #include "c3_internal.h"
 
@@ -42,12 +45,29 @@ __device__ __forceinline__ void st_vec(uint8_t* p, uint4 v) {
                  "r"(v.w)
                  : "memory");
 }
+// Streaming forms: no L1 allocation, L2 lines marked evict-first, so the
+// collective's bytes (touched once) do not push a concurrent GEMM's operands
+// out of L2.
+__device__ __forceinline__ uint4 ld_vec_stream(const uint8_t* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_vec_stream(uint8_t* p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
 
 // Work unit of the vec kernel: a "round" of kVecThreads * kVecUnroll vectors
 // (64 KiB) inside one segment.  Rounds are dealt to CTAs grid-stride.
+template <bool kStream>
 __global__ void __launch_bounds__(kVecThreads, 2)
     copy_vec_kernel(SegTable t, DevStatus* st) {
     if (threadIdx.x == 0) stamp_begin(st, false);
+    const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
     constexpr uint64_t kRound = (uint64_t)kVecThreads * kVecUnroll;
     const uint64_t rounds_per_seg = (vecs_per_seg + kRound - 1) / kRound;
@@ -61,12 +81,17 @@ __global__ void __launch_bounds__(kVecThreads, 2)
 #pragma unroll
         for (int u = 0; u < kVecUnroll; ++u) {
             const uint64_t i = v0 + (uint64_t)u * kVecThreads;
-            if (i < vecs_per_seg) v[u] = ld_vec(src + (i << 4));
+            if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
         }
 #pragma unroll
         for (int u = 0; u < kVecUnroll; ++u) {
             const uint64_t i = v0 + (uint64_t)u * kVecThreads;
-            if (i < vecs_per_seg) st_vec(dst + (i << 4), v[u]);
+            if (i < vecs_per_seg) {
+                if (kStream)
+                    st_vec_stream(dst + (i << 4), v[u], pol);
+                else
+                    st_vec(dst + (i << 4), v[u]);
+            }
         }
     }
     __syncthreads();
@@ -76,6 +101,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
 // bulk kernel: chunk c of the collective is segment c / chunks_per_seg at
 // byte offset (c % chunks_per_seg) * kBulkChunk (the last chunk of a segment
 // may be shorter; every size is a multiple of 16 bytes).
+template <bool kStream>
 __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, DevStatus* st) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kBulkBufs];
@@ -90,6 +116,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
     }
     __syncthreads();
     if (threadIdx.x == 0) {
+        const uint64_t pol = kStream ? policy_evict_first() : 0;
         const uint64_t chunks_per_seg = (t.seg_bytes + kBulkChunk - 1) / kBulkChunk;
         const uint64_t total = chunks_per_seg * (uint64_t)t.nseg;
         const uint64_t n_my = (blockIdx.x < total) ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -110,7 +137,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
             const int b = (int)(i % kBulkBufs);
             const uint32_t bar = smem_addr(&full_bar[b]);
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_load(base + (uint32_t)b * kBulkChunk, src, bytes, bar);
+            if (kStream)
+                bulk_load_hint(base + (uint32_t)b * kBulkChunk, src, bytes, bar, pol);
+            else
+                bulk_load(base + (uint32_t)b * kBulkChunk, src, bytes, bar);
         };
         const uint64_t pro = n_my < (uint64_t)kBulkBufs ? n_my : (uint64_t)kBulkBufs;
         for (uint64_t i = 0; i < pro; ++i) issue_load(i);
@@ -126,7 +156,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
             uint8_t* dst;
             uint32_t bytes;
             chunk_of(i, src, dst, bytes);
-            bulk_store(dst, base + (uint32_t)b * kBulkChunk, bytes);
+            if (kStream)
+                bulk_store_hint(dst, base + (uint32_t)b * kBulkChunk, bytes, pol);
+            else
+                bulk_store(dst, base + (uint32_t)b * kBulkChunk, bytes);
             bulk_commit();
             // Refill the buffer of chunk i-1 once its store has read it.
             if (i >= 1 && i - 1 + kBulkBufs < n_my) {
@@ -154,26 +187,35 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
 // ---------------------------------------------------------------- host side
 
 int copy_init_device(int max_reserve) {
-    cudaError_t e = cudaFuncSetAttribute(copy_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kBulkSmem);
-    if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_bulk_kernel)");
-    if (max_reserve > 0) {
-        e = cudaFuncSetAttribute(copy_vec_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 max_reserve);
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_vec_kernel)");
+    cudaError_t e = cudaSuccess;
+    for (auto fn : {copy_bulk_kernel<false>, copy_bulk_kernel<true>}) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_bulk_kernel)");
     }
+    if (max_reserve > 0)
+        for (auto fn : {copy_vec_kernel<false>, copy_vec_kernel<true>}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_reserve);
+            if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_vec_kernel)");
+        }
     return 0;
 }
 
-int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, cudaStream_t s,
+int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, int l2_stream, cudaStream_t s,
                    DevStatus* st, int* ctas_out) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
     if (ctas < 1) ctas = 1;
-    if (flavour == kSmkBulk)
-        copy_bulk_kernel<<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st);
-    else
-        copy_vec_kernel<<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+    if (flavour == kSmkBulk) {
+        if (l2_stream)
+            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st);
+        else
+            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st);
+    } else {
+        if (l2_stream)
+            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+        else
+            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "copy kernel launch");
     count_launch();

@@ -73,6 +73,14 @@ typedef enum {
  * through a shared-memory ring, one CTA per SM. */
 typedef enum { C3_SMK_AUTO = 0, C3_SMK_VEC = 1, C3_SMK_BULK = 2 } c3_sm_kernel;
 
+/* L2 treatment of the SM collective's loads and stores.  NORMAL: default
+ * caching.  EVICT_FIRST: no L1 allocation and an L2 evict-first policy, so the
+ * bytes the collective touches once do not displace a concurrent GEMM's
+ * operands -- the software counterpart of the pages' point that DMA transfers
+ * bypass the caches ("What carries the argument"; Sections II-A, VI-A).
+ * Copy engines ignore it. */
+typedef enum { C3_L2_NORMAL = 0, C3_L2_EVICT_FIRST = 1 } c3_l2_policy;
+
 /* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
 typedef enum { C3_CLASS_G_LONG = 0, C3_CLASS_GC_EQUAL = 1, C3_CLASS_C_LONG = 2 } c3_class;
 
@@ -174,6 +182,7 @@ typedef struct {
     int nranks;
     int comm_sms;              /* SM budget of the un-partitioned SM collective (0 = default) */
     int sm_kernel;             /* c3_sm_kernel */
+    int coll_l2;               /* c3_l2_policy of the SM collective */
     /* optional L2 flush between the phases of c3_time (caller-owned scratch,
      * larger than L2; NULL = no flush) */
     void *flush_buf;

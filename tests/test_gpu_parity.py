@@ -164,11 +164,24 @@ def test_sm_kernel_flavours_bit_exact(c3):
     ds = [dev_bytes(s) for s in shards]
     for smk in (c3.C3_SMK_VEC, c3.C3_SMK_BULK):
         for split in (0, 16):
-            dC = torch.full((w.M, w.N), float("nan"), device="cuda")
-            out = torch.zeros(w.coll_bytes, dtype=torch.uint8, device="cuda")
-            p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLGATHER, out, w.unit_bytes, 8,
-                           shards=ds, sm_kernel=smk)
-            t = c3.c3_run(p, c3.C3_MODE_CONCURRENT_SM, split, 0)
-            assert t["status"] == 0
-            assert np.array_equal(out.cpu().numpy(), ref), (smk, split)
-            assert_gemm_close(dC.cpu().numpy(), C_ref, S_ref)
+            for l2 in (c3.C3_L2_NORMAL, c3.C3_L2_EVICT_FIRST):
+                dC = torch.full((w.M, w.N), float("nan"), device="cuda")
+                out = torch.zeros(w.coll_bytes, dtype=torch.uint8, device="cuda")
+                p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLGATHER, out, w.unit_bytes, 8,
+                               shards=ds, sm_kernel=smk, coll_l2=l2)
+                t = c3.c3_run(p, c3.C3_MODE_CONCURRENT_SM, split, 0)
+                assert t["status"] == 0
+                assert np.array_equal(out.cpu().numpy(), ref), (smk, split, l2)
+                assert_gemm_close(dC.cpu().numpy(), C_ref, S_ref)
+
+
+@pytest.mark.parametrize("l2", [0, 1])
+def test_alltoall_streaming_variants_bit_exact(c3, l2):
+    w = I.WORKLOADS["tiny_a2a"]
+    send = I.coll_payload(w)
+    d_in = dev_bytes(send)
+    out = torch.zeros(w.coll_bytes, dtype=torch.uint8, device="cuda")
+    p = c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLTOALL, out, w.unit_bytes, 8, send=d_in,
+                   sm_kernel=c3.C3_SMK_BULK, comm_sms=7, coll_l2=l2)
+    c3.c3_run(p, c3.C3_MODE_SERIAL_SM, 0, 0)
+    assert np.array_equal(out.cpu().numpy(), oracle.alltoall(send, 8))
