@@ -72,8 +72,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
     ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
+    ap.add_argument("--ce-variant", choices=["per_segment", "strided", "graph"], default="graph",
+                    help="how the copy-engine modes issue their transfers")
     ap.add_argument("--coll-l2", choices=["normal", "evict_first"], default="normal",
                     help="L2 policy of the SM collective's loads and stores")
+    ap.add_argument("--heuristics", action="store_true",
+                    help="instead of the headline line: calibrate the SM-split slowdown table once, then compare the "
+                         "split the pages' heuristic predicts with the swept best over the size sweep")
     ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
                     help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
     return ap.parse_args(argv)
@@ -365,6 +370,10 @@ def coll_l2_arg(args, c3):
     return c3.C3_L2_EVICT_FIRST if args.coll_l2 == "evict_first" else c3.C3_L2_NORMAL
 
 
+def ce_variant_arg(args, c3):
+    return {"per_segment": c3.C3_CE_PER_SEGMENT, "strided": c3.C3_CE_STRIDED, "graph": c3.C3_CE_GRAPH}[args.ce_variant]
+
+
 def run_sweep(args, c3, torch, np, I, dev, info):
     """The pages' size sweep: an 8192^3 GEMM against collectives of 1 MiB to
     1 GiB total (x2 steps), every mode of --modes (default: baseline,
@@ -390,7 +399,8 @@ def run_sweep(args, c3, torch, np, I, dev, info):
             ref = oracle.alltoall(payload, w.nranks)
         out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
         prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, cid, out, w.unit_bytes, w.nranks, shards=dsh, send=dsend,
-                          flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3))
+                          flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
+                          ce_variant=ce_variant_arg(args, c3))
         per = {m[0]: [] for m in modes}
         for it in range(args.warmup + args.steps):
             for name, mode, split, prio in modes:
@@ -417,6 +427,102 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     return 0
 
 
+def run_heuristics(args, c3, torch, np, I, dev, info):
+    """Validation of the resource-partitioning heuristic (pages, Section V-C:
+    a one-time slowdown table plus a 0.70-efficiency roofline; 24 of 30
+    scenarios predicted, at most 1.5% loss).  Timing only: operands are
+    device-random, outputs are not checked here (parity is the tests' job)."""
+    peaks = load_peaks()
+    S = info["sm_count"]
+    ks = [8, 16, 32, 64]
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+
+    def med_time(fn, reps=7):
+        ts = []
+        for _ in range(reps + 1):
+            c3.c3_l2_flush(flush, flush.numel(), stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts[1:])
+
+    def operands(M, N, K):
+        A = torch.randn((M, K), device=dev, generator=g).to(torch.bfloat16)
+        B = (0.02 * torch.randn((N, K), device=dev, generator=g)).to(torch.bfloat16)
+        return A, B, torch.empty((M, N), dtype=torch.float32, device=dev)
+
+    # ---- one-time table
+    slow = {}
+    for label, (M, N, K) in (("compute", (8192, 8192, 8192)), ("memory", (256, 28672, 8192))):
+        A, B, C = operands(M, N, K)
+        base = med_time(lambda: c3.c3_gemm(A, B, C, M, N, K, 0, stream))
+        slow[label] = [med_time(lambda: c3.c3_gemm(A, B, C, M, N, K, S - k, stream)) / base for k in ks]
+        del A, B, C
+    unit = (256 << 20) // 8
+    shards = [torch.empty(unit, dtype=torch.uint8, device=dev) for _ in range(8)]
+    out = torch.empty(8 * unit, dtype=torch.uint8, device=dev)
+
+    def coll_time(k):
+        p = c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLGATHER, out, unit, 8, shards=shards, comm_sms=k,
+                       sm_kernel=c3.C3_SMK_BULK, stream=stream)
+        ts = []
+        for _ in range(6):
+            c3.c3_l2_flush(flush, flush.numel(), stream)
+            ts.append(c3.c3_run(p, c3.C3_MODE_SERIAL_SM, 0, 0)["t_conc"])
+        return statistics.median(ts[1:])
+
+    cbase = coll_time(S)
+    slow["coll"] = [coll_time(k) / cbase for k in ks]
+    del shards, out
+    table = [(k, slow["compute"][i], slow["memory"][i], slow["coll"][i]) for i, k in enumerate(ks)]
+
+    # ---- scenarios: the size sweep (both collectives) and the memory-bound workload
+    scen = [(w.name, w) for coll in ("allgather", "alltoall") for w in I.sweep_workloads(coll)]
+    scen.append(("mem_ag", I.WORKLOADS["mem_ag"]))
+    rows, hits = [], 0
+    cache = {}
+    for name, w in scen:
+        key = (w.M, w.N, w.K)
+        if key not in cache:
+            cache.clear()
+            cache[key] = operands(w.M, w.N, w.K)
+        A, B, C = cache[key]
+        if w.coll == "allgather":
+            sh = [torch.randint(0, 255, (w.unit_bytes,), dtype=torch.uint8, device=dev) for _ in range(8)]
+            send, cid = None, c3.C3_COLL_ALLGATHER
+        else:
+            sh, send, cid = None, torch.randint(0, 255, (w.coll_bytes,), dtype=torch.uint8, device=dev), \
+                c3.C3_COLL_ALLTOALL
+        o = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
+        p = c3.Problem(A, B, C, w.M, w.N, w.K, cid, o, w.unit_bytes, w.nranks, shards=sh, send=send, stream=stream)
+        meas = {}
+        for k in ks:
+            ts = []
+            for _ in range(5):
+                c3.c3_l2_flush(flush, flush.numel(), stream)
+                ts.append(c3.c3_run(p, c3.C3_MODE_CONCURRENT_SM, k, 0)["t_conc"])
+            meas[k] = statistics.median(ts[1:])
+        best_k = min(meas, key=meas.get)
+        pk, pt, _ = c3.c3_rp_predict(table, w.gemm_flops, w.gemm_bytes, w.coll_bytes, peaks["bf16_tflops"] * 1e12,
+                                     peaks["hbm_gbs"] * 1e9)
+        loss = meas[pk] / meas[best_k] - 1.0
+        hit = pk == best_k or loss <= 0.015
+        hits += hit
+        rows.append({"scenario": name, "best_sms": best_k, "predicted_sms": pk, "loss_pct": 100 * loss, "hit": hit,
+                     "t_conc_us": {str(k): 1e6 * v for k, v in meas.items()}})
+        del sh, send, o, p
+    print(json.dumps({"heuristics": "rp", "table": [{"sms": k, "gemm_compute": gc, "gemm_memory": gm, "coll": co}
+                                                    for k, gc, gm, co in table],
+                      "scenarios": len(rows), "hits": hits, "rows": rows, "peaks": peaks}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local, pg = dist_init(args)
@@ -436,6 +542,8 @@ def main(argv=None):
     info = c3.c3_get_device_info()
     if args.sweep:
         return run_sweep(args, c3, torch, np, I, dev, info)
+    if args.heuristics:
+        return run_heuristics(args, c3, torch, np, I, dev, info)
     w = I.WORKLOADS[args.workload]
     modes = MODES if not args.modes else [m for m in MODES if m[0] in args.modes.split(",")]
 
@@ -454,7 +562,8 @@ def main(argv=None):
     flush = torch.empty(max(2 * info["l2_bytes"], 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
-                      send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3))
+                      send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
+                          ce_variant=ce_variant_arg(args, c3))
 
     # ---- warm-up steps
     for _ in range(args.warmup):
@@ -553,7 +662,7 @@ def main(argv=None):
                    "collective": f"{w.coll} {w.nranks} ranks x {w.unit_bytes} B",
                    "l2": f"flushed before every timed phase ({flush.numel() >> 20} MiB zero-fill)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "coll_l2": args.coll_l2,
+                   "coll_l2": args.coll_l2, "ce_variant": args.ce_variant,
                    "modes": [m[0] for m in modes]},
         "best_mode": best,
         "gemm_tflops_overlap": stats[best]["gemm_tflops_overlap"],

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libc3.so")
-SOURCES = ["gemm_tcgen05.cu", "coll_copy.cu", "c3_timer.cu", "ce_offload.cpp", "c3_runtime.cpp"]
+SOURCES = ["gemm_tcgen05.cu", "coll_copy.cu", "c3_timer.cu", "ce_offload.cpp", "c3_runtime.cpp", "heuristics.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -21,6 +21,7 @@ C3_COLL_ALLGATHER, C3_COLL_ALLTOALL = 0, 1
 C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_CE = 0, 1, 2, 3
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
+C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH = 0, 1, 2
 CLASS_NAMES = {0: "G-long", 1: "GC-equal", 2: "C-long"}
 
 _i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -36,6 +37,7 @@ class C3Problem(ctypes.Structure):
     _fields_ = [("A", _vp), ("B", _vp), ("C", _vp), ("M", _i64), ("N", _i64), ("K", _i64),
                 ("coll", _int), ("shards", ctypes.POINTER(_vp)), ("send", _vp), ("recv", _vp),
                 ("unit_bytes", _sz), ("nranks", _int), ("comm_sms", _int), ("sm_kernel", _int), ("coll_l2", _int),
+                ("ce_variant", _int),
                 ("flush_buf", _vp), ("flush_bytes", _sz), ("stream", _vp)]
 
 
@@ -53,6 +55,14 @@ class C3Timing(ctypes.Structure):
         d = {n: getattr(self, n) for n in _TIMING_DOUBLES + _TIMING_INTS}
         d["class"] = CLASS_NAMES.get(self.cls, "?")
         return d
+
+
+C3_RP_MAX = 16
+
+
+class C3RpTable(ctypes.Structure):
+    _fields_ = [("n", _int), ("sms", _int * C3_RP_MAX), ("gemm_compute", ctypes.c_double * C3_RP_MAX),
+                ("gemm_memory", ctypes.c_double * C3_RP_MAX), ("coll", ctypes.c_double * C3_RP_MAX)]
 
 
 class C3Error(RuntimeError):
@@ -80,6 +90,10 @@ def _load():
         "c3_l2_flush": [_vp, _sz, _vp],
         "c3_gemm_noalloc": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _int],
         "c3_selftest_wait": [ctypes.c_uint64, _int, _vp],
+        "c3_sp_predict": [_int, _int],
+        "c3_rp_predict": [ctypes.POINTER(C3RpTable), ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                          ctypes.c_double, ctypes.c_double, ctypes.POINTER(_int), ctypes.POINTER(ctypes.c_double),
+                          ctypes.POINTER(ctypes.c_double)],
         "c3_gemm_plan": [_i64, _i64, _i64, _int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)],
     }
     for name, args in sig.items():
@@ -96,7 +110,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
-            "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait")
+            "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_sp_predict", "c3_rp_predict")
 
 
 def lib():
@@ -192,6 +206,29 @@ def c3_selftest_wait(limit_ns, arrive, stream=None):
     return int(_lib.c3_selftest_wait(int(limit_ns), int(arrive), _stream(stream)))
 
 
+def c3_sp_predict(gemm_ctas, coll_ctas):
+    """1 if the collective should be launched first (fewer CTAs), else 0."""
+    rc = _lib.c3_sp_predict(int(gemm_ctas), int(coll_ctas))
+    if rc < 0:
+        _check(rc, "c3_sp_predict")
+    return rc
+
+
+def c3_rp_predict(table, gemm_flops, gemm_bytes, coll_bytes, peak_flops, peak_bytes_per_s):
+    """table: list of (sms, gemm_compute_slowdown, gemm_memory_slowdown, coll_slowdown).
+    Returns (best_sms, predicted_seconds, [prediction per entry])."""
+    t = C3RpTable()
+    t.n = len(table)
+    for i, (k, gc, gm, co) in enumerate(table):
+        t.sms[i], t.gemm_compute[i], t.gemm_memory[i], t.coll[i] = int(k), float(gc), float(gm), float(co)
+    best, tp = _int(), ctypes.c_double()
+    each = (ctypes.c_double * C3_RP_MAX)()
+    _check(_lib.c3_rp_predict(ctypes.byref(t), float(gemm_flops), float(gemm_bytes), float(coll_bytes),
+                              float(peak_flops), float(peak_bytes_per_s), ctypes.byref(best), ctypes.byref(tp),
+                              each), "c3_rp_predict")
+    return best.value, tp.value, [each[i] for i in range(t.n)]
+
+
 def c3_l2_flush(buf, nbytes, stream=None):
     return _check(_lib.c3_l2_flush(_ptr(buf), int(nbytes), _stream(stream)), "c3_l2_flush")
 
@@ -200,14 +237,16 @@ class Problem:
     """Owns the ctypes problem record and keeps the host shard-pointer array alive."""
 
     def __init__(self, A, B, C, M, N, K, coll, recv, unit_bytes, nranks=8, shards=None, send=None,
-                 comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None, coll_l2=C3_L2_NORMAL):
+                 comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None, coll_l2=C3_L2_NORMAL,
+                 ce_variant=C3_CE_PER_SEGMENT):
         self._shard_arr = None
         if shards is not None:
             self._shard_arr = (_vp * len(shards))(*[_ptr(s) for s in shards])
         fb, fn = (None, 0) if flush is None else (_ptr(flush), flush.numel() * flush.element_size())
         self.rec = C3Problem(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(coll),
                              self._shard_arr, _ptr(send), _ptr(recv), int(unit_bytes), int(nranks),
-                             int(comm_sms), int(sm_kernel), int(coll_l2), fb, fn, _stream(stream))
+                             int(comm_sms), int(sm_kernel), int(coll_l2), int(ce_variant), fb, fn,
+                             _stream(stream))
 
 
 def c3_run(problem: Problem, mode, sm_split=0, priority=0, check=True):

@@ -38,13 +38,19 @@ static_assert(sizeof(DevStatus) <= kStatusBytes, "status block too small");
 constexpr int kMaxSegs = 64;
 
 // A collective as a list of equal-size byte segments src[i] -> dst[i].
+enum { kSegAllGather = 0, kSegAllToAll = 1 };
+
 struct SegTable {
     const uint8_t* src[kMaxSegs];
     uint8_t* dst[kMaxSegs];
     int nseg;
-    int pad;
+    int kind;       // kSegAllGather or kSegAllToAll
     uint64_t seg_bytes;
+    int nranks;
+    int pad;
 };
+
+enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2 };
 
 enum { kSmkVec = 1, kSmkBulk = 2 };
 
@@ -59,6 +65,7 @@ struct DeviceState {
     cudaStream_t s_gemm = nullptr;     // default priority
     cudaStream_t s_comm = nullptr;     // default priority
     cudaStream_t s_comm_hi = nullptr;  // highest priority
+    cudaStream_t s_capture = nullptr;  // private stream for capturing copy-engine graphs
     cudaEvent_t ev[8] = {};
     DevStatus* status = nullptr;       // device status block
     bool ready = false;
@@ -87,7 +94,8 @@ int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, i
 int copy_init_device(int max_reserve);
 int bulk_copy_smem_bytes();
 
-int copy_ce_launch(const SegTable& t, cudaStream_t s);
+int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream);
+void ce_release_graphs(int device);
 
 int status_reset_launch(DevStatus* st, cudaStream_t s);
 int selftest_wait_launch(DevStatus* st, unsigned long long limit_ns, int arrive, cudaStream_t s);

@@ -70,6 +70,7 @@ static int init_device(DeviceState& ds, int dev) {
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_gemm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
+    C3_TRY(cudaStreamCreateWithFlags(&ds.s_capture, cudaStreamNonBlocking), "stream");
     for (auto& ev : ds.ev) C3_TRY(cudaEventCreate(&ev), "event");
     C3_TRY(cudaMalloc(reinterpret_cast<void**>(&ds.status), kStatusBytes), "status block");
     C3_TRY(cudaMemset(ds.status, 0, kStatusBytes), "status block");
@@ -86,6 +87,8 @@ static void release_device(DeviceState& ds) {
     if (ds.s_gemm) cudaStreamDestroy(ds.s_gemm);
     if (ds.s_comm) cudaStreamDestroy(ds.s_comm);
     if (ds.s_comm_hi) cudaStreamDestroy(ds.s_comm_hi);
+    if (ds.s_capture) cudaStreamDestroy(ds.s_capture);
+    if (ds.device >= 0) ce_release_graphs(ds.device);
     for (auto& ev : ds.ev)
         if (ev) cudaEventDestroy(ev);
     if (ds.status) cudaFree(ds.status);
@@ -168,6 +171,8 @@ static int build_allgather(const void* const* shards, void* out, size_t shard_by
         t->dst[r] = static_cast<uint8_t*>(out) + (size_t)r * shard_bytes;
     }
     t->nseg = nranks;
+    t->kind = kSegAllGather;
+    t->nranks = nranks;
     t->seg_bytes = shard_bytes;
     return C3_OK;
 }
@@ -186,16 +191,18 @@ static int build_alltoall(const void* in, void* out, size_t block_bytes, int nra
             t->dst[i * nranks + j] = static_cast<uint8_t*>(out) + (size_t)(j * nranks + i) * block_bytes;
         }
     t->nseg = nranks * nranks;
+    t->kind = kSegAllToAll;
+    t->nranks = nranks;
     t->seg_bytes = block_bytes;
     return C3_OK;
 }
 
 // One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
 // the CTAs keep their SMs to themselves (partitioning).
-static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int l2_stream, int budget,
-                       bool exclusive, cudaStream_t s, int* ctas) {
+static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int l2_stream, int ce_variant,
+                       int budget, bool exclusive, cudaStream_t s, int* ctas) {
     if (ctas) *ctas = 0;
-    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, s);
+    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
     int k = budget > 0 ? budget : default_comm_sms(ds);
     if (k > ds.sm_count) k = ds.sm_count;
     int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
@@ -281,6 +288,7 @@ static int check_problem(const c3_problem* p, SegTable* t) {
     if (rc) return rc;
     if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
     if (p->coll_l2 != C3_L2_NORMAL && p->coll_l2 != C3_L2_EVICT_FIRST) return set_error(C3_EINVAL, "bad coll_l2");
+    if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH) return set_error(C3_EINVAL, "bad ce_variant");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
     if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
     const size_t cb = t->seg_bytes * (size_t)t->nseg;
@@ -306,7 +314,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int
         rc = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds.status, &gctas);
         if (rc) return rc;
         if ((e = cudaEventRecord(ev_g, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
-        rc = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, &cctas);
+        rc = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, &cctas);
         if (rc) return rc;
         if ((e = cudaEventRecord(ev_c, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     } else {
@@ -320,7 +328,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
         auto go_gemm = [&] { return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, gemm_budget, sg, ds.status, &gctas); };
-        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, comm_budget, part, sc, &cctas); };
+        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas); };
         if (priority) {
             if ((rc = go_comm())) return rc;
             if ((rc = go_gemm())) return rc;
@@ -468,7 +476,7 @@ int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int n
     if (shard_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int engine, int sm_budget,
@@ -481,7 +489,7 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     if (block_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s) {
@@ -549,12 +557,12 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
         });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_comm_iso, [&] {
-            return launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, nullptr);
+            return launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_serial_meas, [&] {
             int r1 = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
-            return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->comm_sms, false, s0, nullptr);
+            return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
         if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;

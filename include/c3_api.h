@@ -81,6 +81,17 @@ typedef enum { C3_SMK_AUTO = 0, C3_SMK_VEC = 1, C3_SMK_BULK = 2 } c3_sm_kernel;
  * Copy engines ignore it. */
 typedef enum { C3_L2_NORMAL = 0, C3_L2_EVICT_FIRST = 1 } c3_l2_policy;
 
+/* How the copy-engine path issues its transfers.  PER_SEGMENT: one
+ * device-to-device cudaMemcpyAsync per segment (8 for the all-gather, R^2 for
+ * the all-to-all).  STRIDED: the all-to-all as R cudaMemcpy2DAsync calls, one
+ * per source rank (all-gathers as PER_SEGMENT).  GRAPH: the STRIDED calls
+ * captured once into a CUDA graph, cached by buffer addresses and size (up to
+ * 16 graphs, released by c3_shutdown), replayed with one launch.  The pages'
+ * DMA collectives lose to the compute-unit library below 32 MB on launch and
+ * synchronisation cost (Figure 9); STRIDED and GRAPH cut the number of host
+ * calls per collective. */
+typedef enum { C3_CE_PER_SEGMENT = 0, C3_CE_STRIDED = 1, C3_CE_GRAPH = 2 } c3_ce_variant;
+
 /* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
 typedef enum { C3_CLASS_G_LONG = 0, C3_CLASS_GC_EQUAL = 1, C3_CLASS_C_LONG = 2 } c3_class;
 
@@ -183,6 +194,7 @@ typedef struct {
     int comm_sms;              /* SM budget of the un-partitioned SM collective (0 = default) */
     int sm_kernel;             /* c3_sm_kernel */
     int coll_l2;               /* c3_l2_policy of the SM collective */
+    int ce_variant;            /* c3_ce_variant of the copy-engine collective */
     /* optional L2 flush between the phases of c3_time (caller-owned scratch,
      * larger than L2; NULL = no flush) */
     void *flush_buf;
@@ -294,6 +306,40 @@ int c3_gemm_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N
  * library's own).
  */
 int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s);
+
+/*
+ * Runtime heuristics of the pages (Section V-C).
+ *
+ * c3_sp_predict: schedule prioritisation -- returns 1 when the collective
+ * should be launched first (it has fewer CTAs than the GEMM), else 0; the
+ * pages' rule is to launch the lower-workgroup-count kernel first.
+ *
+ * c3_rp_predict: resource partitioning from a one-time slowdown table (the
+ * pages' Figure 5) and a roofline at 70% efficiency.  Entry i of the table
+ * says: with sms[i] SMs given to the collective, a compute-bound GEMM runs
+ * gemm_compute[i] times slower than on every SM, a memory-bound GEMM
+ * gemm_memory[i] times slower, and the collective coll[i] times slower than
+ * on every SM.  The isolated times are taken from the roofline (GEMM:
+ * max(flops / (0.7 * peak_flops), bytes / (0.7 * peak_bw)); collective:
+ * 2 * coll_bytes / (0.7 * peak_bw)); the prediction for entry i is the larger
+ * of the two scaled times; the entry with the smallest prediction wins.
+ * Returns its SM count in *best_sms and its predicted time (s) in
+ * *t_pred_best; t_pred_each (may be NULL) receives all n predictions.  Host
+ * only; C3_EINVAL on empty tables, non-positive entries or sizes.
+ */
+#define C3_RP_MAX 16
+typedef struct {
+    int n;
+    int sms[C3_RP_MAX];
+    double gemm_compute[C3_RP_MAX];
+    double gemm_memory[C3_RP_MAX];
+    double coll[C3_RP_MAX];
+} c3_rp_table;
+
+int c3_sp_predict(int gemm_ctas, int coll_ctas);
+int c3_rp_predict(const c3_rp_table *t, double gemm_flops, double gemm_bytes, double coll_bytes,
+                  double peak_flops, double peak_bytes_per_s, int *best_sms, double *t_pred_best,
+                  double *t_pred_each);
 
 /* Writes `bytes` of zeros over `buf` (device) with an SM kernel: the L2 flush
  * used between timed phases.  Asynchronous on `s`. */

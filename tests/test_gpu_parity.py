@@ -185,3 +185,26 @@ def test_alltoall_streaming_variants_bit_exact(c3, l2):
                    sm_kernel=c3.C3_SMK_BULK, comm_sms=7, coll_l2=l2)
     c3.c3_run(p, c3.C3_MODE_SERIAL_SM, 0, 0)
     assert np.array_equal(out.cpu().numpy(), oracle.alltoall(send, 8))
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("coll,unit", [("allgather", 1 << 20), ("allgather", 4096 + 48),
+                                       ("alltoall", 128 * 1024), ("alltoall", 1024 + 16)])
+def test_copy_engine_variants_bit_exact(c3, variant, coll, unit):
+    # per-segment copies, strided 2-D copies, and a cached CUDA graph of the copies;
+    # run twice so the graph variant also replays its cached graph
+    if coll == "allgather":
+        payload = [I.random_bytes(1002 + r, unit) for r in range(8)]
+        ref = oracle.allgather(payload)
+        ds = [dev_bytes(x) for x in payload]
+        send, cid = None, c3.C3_COLL_ALLGATHER
+    else:
+        payload = I.random_bytes(1002, 64 * unit)
+        ref = oracle.alltoall(payload, 8)
+        ds, send, cid = None, dev_bytes(payload), c3.C3_COLL_ALLTOALL
+    out = torch.zeros(ref.size, dtype=torch.uint8, device="cuda")
+    p = c3.Problem(None, None, None, 0, 0, 0, cid, out, unit, 8, shards=ds, send=send, ce_variant=variant)
+    for _ in range(2):
+        out.fill_(0x33)
+        c3.c3_run(p, c3.C3_MODE_SERIAL_CE, 0, 0)
+        assert np.array_equal(out.cpu().numpy(), ref)
