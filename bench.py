@@ -308,7 +308,12 @@ def cpu_c3(w, steps, warmup, rows=None, target_s=1.0):
     A = A_rows(rows)
     frac = rows / w.M
     unit = max(16, int(w.unit_bytes * frac) // 16 * 16)
-    if w.coll == "allgather":
+    if w.coll == "allreduce":
+        cnt = max(w.nranks * 4, int(w.unit_bytes * frac) // 4 // (w.nranks * 4) * (w.nranks * 4))
+        vecs = [I.normal(1002 + r, cnt).astype(np.float32) for r in range(w.nranks)]
+        unit = 4 * cnt
+        coll = lambda: oracle.allreduce(vecs)  # noqa: E731
+    elif w.coll == "allgather":
         shards = [I.random_bytes(1002 + r, unit) for r in range(w.nranks)]
         coll = lambda: oracle.allgather(shards)  # noqa: E731
     else:
@@ -325,7 +330,7 @@ def cpu_c3(w, steps, warmup, rows=None, target_s=1.0):
         if it >= warmup:
             recs.append((tg, tc, tconc))
     sample = (f"{rows} of {w.M} rows of A against all {w.N}x{w.K} of B (oracle fp64 GEMM, {g_threads} threads) "
-              f"and {unit} B per {'shard' if w.coll == 'allgather' else 'block'} ({frac:.4f} of the "
+              f"and {unit} B per {dict(allgather='shard', alltoall='block').get(w.coll, 'rank vector')} ({frac:.4f} of the "
               f"collective, oracle byte loop, 1 thread), isolated then concurrent")
     return recs, sample, cores
 
@@ -553,9 +558,10 @@ def main(argv=None):
     dA = torch.from_numpy(A_h.view(np.int16)).to(dev)
     dB = torch.from_numpy(B_h.view(np.int16)).to(dev)
     dC = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
-    if w.coll == "allgather":
+    if w.coll in ("allgather", "allreduce"):
         dshards = [torch.from_numpy(s).to(dev) for s in payload]
-        dsend, coll_id = None, c3.C3_COLL_ALLGATHER
+        dsend = None
+        coll_id = c3.C3_COLL_ALLGATHER if w.coll == "allgather" else c3.C3_COLL_ALLREDUCE
     else:
         dshards, dsend, coll_id = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
     out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
@@ -591,7 +597,10 @@ def main(argv=None):
 
     # ---- post-run validation (every mode ran on these buffers; check the last outputs)
     import oracle
-    if w.coll == "allgather":
+    if w.coll == "allreduce":
+        coll_ok = bool(np.array_equal(out.cpu().numpy().view(np.uint32),
+                                      oracle.allreduce(payload)[0].reshape(-1).view(np.uint32)))
+    elif w.coll == "allgather":
         coll_ok = bool(np.array_equal(out.cpu().numpy(), np.concatenate(payload)))
     else:
         coll_ok = bool(np.array_equal(out.cpu().numpy(), oracle.alltoall(payload, w.nranks)))
@@ -611,7 +620,9 @@ def main(argv=None):
         m = pct_gain(tg, tc_strict, tconc)
         m_own = pct_gain(tg, tc, tconc)
         tgd = statistics.median(r["t_gemm_dev"] for r in recs)
-        tcd = [r["t_comm_dev"] if r["comm_ctas"] else r["t_comm_ev"] for r in recs]
+        # the SM collective's own kernel window when it is all on SMs; fork-to-done
+        # events when copy engines carry all or part of it
+        tcd = [r["t_comm_dev"] if (r["comm_ctas"] and r["mode"] in (0, 1)) else r["t_comm_ev"] for r in recs]
         stats[name] = {
             "t_gemm_iso_us": 1e6 * tg, "t_comm_iso_us": 1e6 * tc, "t_comm_iso_strict_us": 1e6 * tc_strict,
             "t_conc_us": 1e6 * tconc,
@@ -622,7 +633,7 @@ def main(argv=None):
             "pct_ideal_gain_own_engine_per_step": spread([100.0 * r["pct_ideal_gain"] for r in recs]),
             "class": recs[0]["class"],
             "gemm_tflops_overlap": w.gemm_flops / tgd / 1e12 if tgd > 0 else None,
-            "copy_gbs_overlap": 2 * w.coll_bytes / statistics.median(tcd) / 1e9 if statistics.median(tcd) > 0 else None,
+            "copy_gbs_overlap": w.coll_traffic_bytes / statistics.median(tcd) / 1e9 if statistics.median(tcd) > 0 else None,
             "gemm_slowdown": tgd / tg if tg > 0 else None,
             "gemm_ctas": recs[0]["gemm_ctas"], "comm_ctas": recs[0]["comm_ctas"],
             "smid_overlap_max": max(r["smid_overlap"] for r in recs),
@@ -650,9 +661,11 @@ def main(argv=None):
     tc_sm = statistics.median(r["t_comm_iso"] for r in per_mode["baseline"]) if "baseline" in per_mode else None
     copy_roof = None
     if tc_sm:
-        gbs = 2 * w.coll_bytes / tc_sm / 1e9
+        gbs = w.coll_traffic_bytes / tc_sm / 1e9
         copy_roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "kernel": "copy_vec_kernel (default budget)"}
+                     "frac": gbs / peaks["hbm_gbs"],
+                     "kernel": ("reduce_scatter_kernel + copy_vec_kernel" if w.coll == "allreduce"
+                                else "copy_vec_kernel") + " (default budget)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -730,7 +743,7 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
         res["gemm"][f"{M}x{N}x{K}"] = {"us": 1e6 * t, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
                                         "plan": list(c3.c3_gemm_plan(M, N, K, 0))}
         del A, B, C
-    if dshards is not None:
+    if dshards is not None and w.coll == "allgather":
         nbytes = 2 * w.coll_bytes
         for kind, smk in (("vec", c3.C3_SMK_VEC), ("bulk", c3.C3_SMK_BULK)):
             res["copy_gbs_by_sms"][kind] = {}
@@ -774,7 +787,7 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
         dpay = [dsend]
     hC = torch.empty(dC.shape, dtype=torch.float32).pin_memory()
     bi_a = hA.numel() * 2
-    bi_p = sum(h.numel() for h in hpay)
+    bi_p = sum(h.numel() * h.element_size() for h in hpay)
     bo = hC.numel() * 4
 
     def h2d_a():
@@ -788,7 +801,9 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
         hC.copy_(dC, non_blocking=True)
 
     def coll():
-        if dshards is not None:
+        if w.coll == "allreduce":
+            c3.c3_allreduce(dshards, out, w.unit_bytes // 4, w.nranks, engine=engine, stream=stream)
+        elif dshards is not None:
             c3.c3_allgather(dshards, out, w.unit_bytes, w.nranks, engine=engine, stream=stream)
         else:
             c3.c3_alltoall(dsend, out, w.unit_bytes, w.nranks, engine=engine, stream=stream)

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libc3.so")
 
 C3_OK, C3_EINVAL, C3_EALIGN, C3_ECUDA, C3_ETIMEOUT, C3_EUNSUP = 0, -1, -2, -3, -4, -5
 C3_ENGINE_SM, C3_ENGINE_CE = 0, 1
-C3_COLL_ALLGATHER, C3_COLL_ALLTOALL = 0, 1
+C3_COLL_ALLGATHER, C3_COLL_ALLTOALL, C3_COLL_ALLREDUCE = 0, 1, 2
 C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_CE = 0, 1, 2, 3
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
@@ -85,6 +85,7 @@ def _load():
         "c3_gemm": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp],
         "c3_allgather": [ctypes.POINTER(_vp), _vp, _sz, _int, _int, _int, _vp],
         "c3_alltoall": [_vp, _vp, _sz, _int, _int, _int, _vp],
+        "c3_allreduce": [ctypes.POINTER(_vp), _vp, _sz, _int, _int, _int, _vp],
         "c3_run": [ctypes.POINTER(C3Problem), _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_time": [ctypes.POINTER(C3Problem), _int, _int, _int, _int, _int, ctypes.POINTER(C3Timing)],
         "c3_l2_flush": [_vp, _sz, _vp],
@@ -109,7 +110,7 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
-            "c3_gemm", "c3_allgather", "c3_alltoall", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
+            "c3_gemm", "c3_allgather", "c3_alltoall", "c3_allreduce", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
             "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_sp_predict", "c3_rp_predict")
 
 
@@ -227,6 +228,14 @@ def c3_rp_predict(table, gemm_flops, gemm_bytes, coll_bytes, peak_flops, peak_by
                               float(peak_flops), float(peak_bytes_per_s), ctypes.byref(best), ctypes.byref(tp),
                               each), "c3_rp_predict")
     return best.value, tp.value, [each[i] for i in range(t.n)]
+
+
+def c3_allreduce(inputs, out, count, nranks, engine=C3_ENGINE_SM, sm_budget=0, stream=None, check=True):
+    arr = None
+    if inputs is not None:
+        arr = (_vp * max(1, len(inputs)))(*[_ptr(x) for x in inputs])
+    rc = _lib.c3_allreduce(arr, _ptr(out), int(count), int(nranks), int(engine), int(sm_budget), _stream(stream))
+    return _check(rc, "c3_allreduce") if check else rc
 
 
 def c3_l2_flush(buf, nbytes, stream=None):

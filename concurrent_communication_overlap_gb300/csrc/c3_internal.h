@@ -38,7 +38,21 @@ static_assert(sizeof(DevStatus) <= kStatusBytes, "status block too small");
 constexpr int kMaxSegs = 64;
 
 // A collective as a list of equal-size byte segments src[i] -> dst[i].
-enum { kSegAllGather = 0, kSegAllToAll = 1 };
+enum { kSegAllGather = 0, kSegAllToAll = 1, kSegAllReduce = 2 };
+
+constexpr int kMaxRanksAr = 8;
+
+// The reduce-scatter half of an all-reduce of nranks fp32 vectors of `count`
+// elements: chunk c (count / nranks elements) of the rank-order sum goes to
+// row c of `out` (nranks rows of `count` floats).
+struct RsTable {
+    const float* in[kMaxRanksAr];
+    float* out;
+    uint64_t count;
+    uint64_t chunk;
+    int nranks;
+    int pad;
+};
 
 struct SegTable {
     const uint8_t* src[kMaxSegs];
@@ -51,6 +65,14 @@ struct SegTable {
 };
 
 enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2 };
+
+// A collective as launched: an optional reduce-scatter pass on SMs (all-reduce
+// only) followed by the segment copies on the chosen engine.
+struct CollPlan {
+    SegTable seg;
+    RsTable rs;
+    bool has_rs = false;
+};
 
 enum { kSmkVec = 1, kSmkBulk = 2 };
 
@@ -92,6 +114,8 @@ int gemm_init_device();  // function attributes; once per device
 int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, int l2_stream, cudaStream_t s,
                    DevStatus* st, int* ctas_out);
 int copy_init_device(int max_reserve);
+int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStream_t s, DevStatus* st,
+                          int* ctas_out);
 int bulk_copy_smem_bytes();
 
 int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream);

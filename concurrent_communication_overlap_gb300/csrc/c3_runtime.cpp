@@ -197,11 +197,64 @@ static int build_alltoall(const void* in, void* out, size_t block_bytes, int nra
     return C3_OK;
 }
 
+static int build_allreduce(const void* const* inputs, void* out, size_t count, int nranks, CollPlan* cp) {
+    if (nranks < 1 || nranks > kMaxRanksAr) return set_error(C3_EINVAL, "nranks must be 1..8 for the all-reduce");
+    if (!inputs || !out) return set_error(C3_EINVAL, "inputs or out is NULL");
+    if (count % ((size_t)nranks * 4))
+        return set_error(C3_EALIGN, "count must be a multiple of 4 * nranks (16-byte chunks)");
+    if (!aligned16(out)) return set_error(C3_EALIGN, "out must be 16-byte aligned");
+    const size_t row = count * sizeof(float);
+    std::memset(&cp->seg, 0, sizeof cp->seg);
+    std::memset(&cp->rs, 0, sizeof cp->rs);
+    for (int q = 0; q < nranks; ++q) {
+        if (!inputs[q]) return set_error(C3_EINVAL, "an input pointer is NULL");
+        if (!aligned16(inputs[q])) return set_error(C3_EALIGN, "inputs must be 16-byte aligned");
+        if (overlaps(inputs[q], row, out, row * (size_t)nranks)) return set_error(C3_EINVAL, "out overlaps an input");
+        cp->rs.in[q] = static_cast<const float*>(inputs[q]);
+    }
+    const size_t chunk = count / (size_t)nranks;
+    float* o = static_cast<float*>(out);
+    cp->rs.out = o;
+    cp->rs.count = count;
+    cp->rs.chunk = chunk ? chunk : 1;
+    cp->rs.nranks = nranks;
+    cp->has_rs = count > 0;
+    int n = 0;
+    for (int c = 0; c < nranks; ++c)
+        for (int r = 0; r < nranks; ++r) {
+            if (r == c) continue;
+            cp->seg.src[n] = reinterpret_cast<const uint8_t*>(o + (size_t)c * count + (size_t)c * chunk);
+            cp->seg.dst[n] = reinterpret_cast<uint8_t*>(o + (size_t)r * count + (size_t)c * chunk);
+            ++n;
+        }
+    cp->seg.nseg = n;
+    cp->seg.kind = kSegAllReduce;
+    cp->seg.nranks = nranks;
+    cp->seg.seg_bytes = chunk * sizeof(float);
+    return C3_OK;
+}
+
 // One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
 // the CTAs keep their SMs to themselves (partitioning).
-static int launch_coll(DeviceState& ds, const SegTable& t, int engine, int sm_kernel, int l2_stream, int ce_variant,
+static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_kernel, int l2_stream, int ce_variant,
                        int budget, bool exclusive, cudaStream_t s, int* ctas) {
     if (ctas) *ctas = 0;
+    const SegTable& t = cp.seg;
+    if (cp.has_rs) {
+        // the reduce-scatter needs arithmetic: always SMs, whatever the engine
+        int k = budget > 0 ? budget : default_comm_sms(ds);
+        if (k > ds.sm_count) k = ds.sm_count;
+        int rc = reduce_scatter_launch(cp.rs, k, exclusive ? exclusive_reserve(ds) : 0, s, ds.status, ctas);
+        if (rc) return rc;
+        if (t.nseg == 0) return 0;
+        int dummy = 0;
+        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
+        int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
+                      : sm_kernel == C3_SMK_BULK ? kSmkBulk
+                      : (exclusive ? kSmkBulk : kSmkVec);
+        int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
+        return copy_sm_launch(t, k, flavour, reserve, l2_stream, s, ds.status, &dummy);
+    }
     if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
     int k = budget > 0 ? budget : default_comm_sms(ds);
     if (k > ds.sm_count) k = ds.sm_count;
@@ -275,15 +328,20 @@ static int read_status(DeviceState& ds, c3_timing* out) {
     return C3_OK;
 }
 
-static int check_problem(const c3_problem* p, SegTable* t) {
+static int check_problem(const c3_problem* p, CollPlan* cp) {
     if (!p) return set_error(C3_EINVAL, "problem is NULL");
     int rc = check_gemm(p->A, p->B, p->C, p->M, p->N, p->K);
     if (rc) return rc;
+    SegTable* t = &cp->seg;
+    cp->has_rs = false;
     if (p->coll == C3_COLL_ALLGATHER)
         rc = build_allgather(p->shards, p->recv, p->unit_bytes, p->nranks, t);
     else if (p->coll == C3_COLL_ALLTOALL)
         rc = build_alltoall(p->send, p->recv, p->unit_bytes, p->nranks, t);
-    else
+    else if (p->coll == C3_COLL_ALLREDUCE) {
+        if (p->unit_bytes % sizeof(float)) return set_error(C3_EALIGN, "all-reduce unit_bytes must hold whole floats");
+        rc = build_allreduce(p->shards, p->recv, p->unit_bytes / sizeof(float), p->nranks, cp);
+    } else
         return set_error(C3_EINVAL, "unknown collective");
     if (rc) return rc;
     if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
@@ -291,7 +349,8 @@ static int check_problem(const c3_problem* p, SegTable* t) {
     if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH) return set_error(C3_EINVAL, "bad ce_variant");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
     if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
-    const size_t cb = t->seg_bytes * (size_t)t->nseg;
+    const size_t cb = p->coll == C3_COLL_ALLREDUCE ? p->unit_bytes * (size_t)p->nranks
+                                                   : t->seg_bytes * (size_t)t->nseg;
     if (overlaps(p->C, (size_t)p->M * (size_t)p->N * 4, p->recv, cb))
         return set_error(C3_EINVAL, "C overlaps the collective's output");
     return C3_OK;
@@ -299,7 +358,7 @@ static int check_problem(const c3_problem* p, SegTable* t) {
 
 // One run of `mode` on already-checked arguments; fills t_conc, the event
 // times and the device facts.
-static int run_once(DeviceState& ds, const c3_problem* p, const SegTable& t, int mode, int sm_split,
+static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int mode, int sm_split,
                     int priority, c3_timing* out) {
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
     cudaEvent_t ev0 = ds.ev[0], ev_g = ds.ev[1], ev_c = ds.ev[2], ev_end = ds.ev[3];
@@ -470,8 +529,8 @@ int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int n
                  int sm_budget, c3_stream s) {
     if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");
     if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
-    SegTable t;
-    int rc = build_allgather(shards, out, shard_bytes, nranks, &t);
+    CollPlan t;
+    int rc = build_allgather(shards, out, shard_bytes, nranks, &t.seg);
     if (rc) return rc;
     if (shard_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
@@ -483,8 +542,8 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
                 c3_stream s) {
     if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");
     if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
-    SegTable t;
-    int rc = build_alltoall(in, out, block_bytes, nranks, &t);
+    CollPlan t;
+    int rc = build_alltoall(in, out, block_bytes, nranks, &t.seg);
     if (rc) return rc;
     if (block_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
@@ -511,6 +570,20 @@ int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s) {
     return status;
 }
 
+int c3_allreduce(const float* const* inputs, float* out, size_t count, int nranks, int engine, int sm_budget,
+                 c3_stream s) {
+    if (engine != C3_ENGINE_SM && engine != C3_ENGINE_CE) return set_error(C3_EINVAL, "unknown engine");
+    if (sm_budget < 0) return set_error(C3_EINVAL, "negative sm_budget");
+    CollPlan t;
+    int rc = build_allreduce(reinterpret_cast<const void* const*>(inputs), out, count, nranks, &t);
+    if (rc) return rc;
+    if (count == 0) return C3_OK;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s),
+                       nullptr);
+}
+
 int c3_l2_flush(void* buf, size_t bytes, c3_stream s) {
     if (!buf && bytes) return set_error(C3_EINVAL, "buf is NULL");
     if (!aligned16(buf)) return set_error(C3_EALIGN, "buf must be 16-byte aligned");
@@ -522,7 +595,7 @@ int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing*
     std::memset(out, 0, sizeof *out);
     if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
     if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
-    SegTable t;
+    CollPlan t;
     int rc = check_problem(p, &t);
     if (rc) return rc;
     DeviceState* ds = device_state();
@@ -541,7 +614,7 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
     if (!per_rep || reps < 1 || warmup < 0) return set_error(C3_EINVAL, "need reps >= 1, warmup >= 0, per_rep");
     if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
     if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
-    SegTable t;
+    CollPlan t;
     int rc = check_problem(p, &t);
     if (rc) return rc;
     DeviceState* ds = device_state();

@@ -184,10 +184,57 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
     __syncthreads();
 }
 
+// Reduce-scatter half of the all-reduce (the part that needs arithmetic and so
+// stays on SMs; the pages offload only the all-gather half to DMA).  Element i
+// of the vector belongs to chunk c = i / chunk; its rank-order fp32 sum
+// ((0 + in_0[i]) + in_1[i]) + ... is written into rank c's output row at
+// position i.  16-byte vectors; all R loads issued before the adds.
+__global__ void __launch_bounds__(kVecThreads, 2) reduce_scatter_kernel(RsTable t, DevStatus* st) {
+    if (threadIdx.x == 0) stamp_begin(st, false);
+    const uint64_t nvec = t.count >> 2;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t v = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        float4 x[kMaxRanksAr];
+#pragma unroll
+        for (int q = 0; q < kMaxRanksAr; ++q)
+            if (q < t.nranks) x[q] = __ldg(reinterpret_cast<const float4*>(t.in[q]) + v);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kMaxRanksAr; ++q)
+            if (q < t.nranks) {
+                acc.x = __fadd_rn(acc.x, x[q].x);
+                acc.y = __fadd_rn(acc.y, x[q].y);
+                acc.z = __fadd_rn(acc.z, x[q].z);
+                acc.w = __fadd_rn(acc.w, x[q].w);
+            }
+        const uint64_t c = (v << 2) / t.chunk;
+        reinterpret_cast<float4*>(t.out + c * t.count)[v] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) stamp_end(st, false);
+}
+
 // ---------------------------------------------------------------- host side
+
+int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStream_t s, DevStatus* st,
+                          int* ctas_out) {
+    if (ctas_out) *ctas_out = 0;
+    if (t.count == 0) return 0;
+    if (ctas < 1) ctas = 1;
+    reduce_scatter_kernel<<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "reduce-scatter launch");
+    count_launch();
+    if (ctas_out) *ctas_out = ctas;
+    return 0;
+}
 
 int copy_init_device(int max_reserve) {
     cudaError_t e = cudaSuccess;
+    if (max_reserve > 0) {
+        e = cudaFuncSetAttribute(reduce_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_reserve);
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(reduce_scatter_kernel)");
+    }
     for (auto fn : {copy_bulk_kernel<false>, copy_bulk_kernel<true>}) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
         if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_bulk_kernel)");

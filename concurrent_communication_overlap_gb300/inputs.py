@@ -145,18 +145,29 @@ class Workload:
     K: int
     a_dist: tuple      # ("uniform", lo, hi) or ("normal", mean, std)
     b_dist: tuple
-    coll: str          # "allgather" or "alltoall"
+    coll: str          # "allgather", "alltoall" or "allreduce"
     nranks: int
-    unit_bytes: int    # shard bytes (all-gather) or block bytes (all-to-all)
+    unit_bytes: int    # shard bytes (all-gather), block bytes (all-to-all), fp32 vector bytes (all-reduce)
     payload: str       # "u16" (random 16-bit patterns) or a bf16 distribution tag
     description: str
 
     @property
     def coll_bytes(self) -> int:
         """Bytes of the collective's output (= bytes of its input)."""
-        if self.coll == "allgather":
+        if self.coll in ("allgather", "allreduce"):
             return self.nranks * self.unit_bytes
         return self.nranks * self.nranks * self.unit_bytes
+
+    @property
+    def coll_traffic_bytes(self) -> int:
+        """Bytes the collective must read and write at least: 2x its size for
+        the copies; for the all-reduce, the reduce-scatter reads every rank's
+        vector and writes one, then the all-gather copies R-1 of R chunks to
+        every rank (read + write)."""
+        if self.coll == "allreduce":
+            row = self.unit_bytes
+            return (self.nranks + 1) * row + 2 * (self.nranks - 1) * row
+        return 2 * self.coll_bytes
 
     @property
     def gemm_flops(self) -> float:
@@ -182,6 +193,13 @@ WORKLOADS = {
                          "allgather", 8, 56 * MiB, "normal0.02",
                          "Llama-70B-FFN-shaped bf16 GEMM 8192x28672x8192 with an 8-rank all-gather "
                          "of an 8192x28672 bf16 weight (8 x 56 MiB)"),
+    "tiny_ar": Workload("tiny_ar", 512, 512, 512, ("uniform", -1.0, 1.0), ("uniform", -1.0, 1.0),
+                        "allreduce", 8, 1 * MiB, "f32normal",
+                        "bf16 GEMM 512^3 (U[-1,1]) with an 8-rank all-reduce of 8 x 1 MiB fp32 vectors"),
+    "mem_ar": Workload("mem_ar", 256, 28672, 8192, ("normal", 0.0, 1.0), ("normal", 0.0, 0.02),
+                       "allreduce", 8, 16 * MiB, "f32normal",
+                       "memory-bound bf16 GEMM 256x28672x8192 with an 8-rank all-reduce of 8 x 16 MiB fp32 "
+                       "gradients (reduce-scatter on SMs, all-gather on the mode's engine)"),
     "l405_a2a": Workload("l405_a2a", 8192, 53248, 16384, ("normal", 0.0, 1.0), ("normal", 0.0, 0.02),
                          "alltoall", 8, 8 * MiB, "u16",
                          "Llama-405B-shaped bf16 GEMM 8192x53248x16384 with an 8x8 all-to-all of "
@@ -218,7 +236,10 @@ def gemm_operands(w: Workload, M=None, N=None, K=None):
 
 def coll_payload(w: Workload):
     """The collective's input: a list of nranks shard byte arrays (all-gather,
-    seeds 1002 + r) or one send buffer of nranks^2 blocks (all-to-all, seed 1002)."""
+    seeds 1002 + r), one send buffer of nranks^2 blocks (all-to-all, seed
+    1002), or nranks fp32 N(0,1) vectors (all-reduce, seeds 1002 + r)."""
+    if w.coll == "allreduce":
+        return [normal(1002 + r, w.unit_bytes // 4).astype(np.float32) for r in range(w.nranks)]
     if w.coll == "allgather":
         shards = []
         for r in range(w.nranks):

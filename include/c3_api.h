@@ -58,7 +58,7 @@ typedef enum {
 } c3_status;
 
 typedef enum { C3_ENGINE_SM = 0, C3_ENGINE_CE = 1 } c3_engine;
-typedef enum { C3_COLL_ALLGATHER = 0, C3_COLL_ALLTOALL = 1 } c3_coll;
+typedef enum { C3_COLL_ALLGATHER = 0, C3_COLL_ALLTOALL = 1, C3_COLL_ALLREDUCE = 2 } c3_coll;
 
 /* How the GEMM and the collective are run (see c3_run). */
 typedef enum {
@@ -177,6 +177,24 @@ int c3_allgather(const void *const *shards, void *out, size_t shard_bytes, int n
 int c3_alltoall(const void *in, void *out, size_t block_bytes, int nranks, int engine,
                 int sm_budget, c3_stream s);
 
+/*
+ * All-reduce of `nranks` fp32 vectors of `count` elements, decomposed the way
+ * the pages propose for DMA offload: a reduce-scatter, which needs arithmetic
+ * and always runs on SMs, then an all-gather of the reduced chunks, which
+ * `engine` carries (C3_ENGINE_CE: copy engines; C3_ENGINE_SM: the SM copy
+ * kernel) (synthesis page, "Attack 1"; pith.science paper page, "Reading
+ * between the lines": a DMA engine has no arithmetic).
+ *   inputs  HOST array of nranks device pointers, count floats each, 16-byte aligned
+ *   out     device, nranks * count floats: row r (out + r*count) is rank r's result
+ *   count   multiple of 4 * nranks (16-byte chunks; else C3_EALIGN); 0 launches nothing
+ *   nranks  1..8
+ * Every row ends as out[r][i] = ((0 + in_0[i]) + in_1[i]) + ... + in_{R-1}[i]
+ * in fp32, rank order -- the same on every row and bit-reproducible.  The
+ * reduce-scatter uses sm_budget SMs (0 = default).  Asynchronous on `s`.
+ */
+int c3_allreduce(const float *const *inputs, float *out, size_t count, int nranks, int engine,
+                 int sm_budget, c3_stream s);
+
 /* One C3 problem: a GEMM and one collective, both on caller-owned buffers. */
 typedef struct {
     /* GEMM (as c3_gemm) */
@@ -186,10 +204,12 @@ typedef struct {
     int64_t M, N, K;
     /* collective */
     int coll;                  /* c3_coll */
-    const void *const *shards; /* all-gather: HOST array of nranks device pointers */
+    const void *const *shards; /* all-gather: HOST array of nranks device pointers (all-reduce: its
+                                  nranks fp32 input vectors) */
     const void *send;          /* all-to-all: send buffer */
     void *recv;                /* output of the collective */
-    size_t unit_bytes;         /* shard bytes (all-gather) or block bytes (all-to-all) */
+    size_t unit_bytes;         /* shard bytes (all-gather), block bytes (all-to-all) or bytes of one
+                                  rank's fp32 vector (all-reduce; recv holds nranks of them) */
     int nranks;
     int comm_sms;              /* SM budget of the un-partitioned SM collective (0 = default) */
     int sm_kernel;             /* c3_sm_kernel */

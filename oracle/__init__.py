@@ -51,6 +51,10 @@ def _load():
             lib.oracle_gemm_entries.argtypes = [vp, vp, i64, i64, i64, vp, vp, i64, vp, vp, ip]
             lib.oracle_allgather.argtypes = [vp, ip, i64, vp]
             lib.oracle_alltoall.argtypes = [vp, ip, i64, vp]
+            lib.oracle_allreduce_f32.argtypes = [vp, ip, i64, vp, vp]
+            lib.oracle_reduce_scatter_f32.argtypes = [vp, ip, i64, vp]
+            lib.oracle_allreduce_f32.restype = ctypes.c_int
+            lib.oracle_reduce_scatter_f32.restype = ctypes.c_int
             lib.oracle_c3_metrics.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double, dp,
                                               ctypes.POINTER(ctypes.c_int)]
             for f in (lib.oracle_gemm, lib.oracle_gemm_entries, lib.oracle_allgather,
@@ -140,6 +144,39 @@ def alltoall(buf, nranks):
     rc = _load().oracle_alltoall(b.ctypes.data, nranks, b.size // (nranks * nranks), out.ctypes.data)
     if rc:
         raise ValueError(f"oracle_alltoall rc={rc}")
+    return out
+
+
+def _f32_list(bufs):
+    bufs = [np.ascontiguousarray(b, np.float32).reshape(-1) for b in bufs]
+    n = bufs[0].size if bufs else 0
+    if any(b.size != n for b in bufs):
+        raise ValueError("rank buffers differ in length")
+    return bufs, n, (ctypes.c_void_p * max(1, len(bufs)))(*[b.ctypes.data for b in bufs])
+
+
+def allreduce(bufs):
+    """All-reduce of R fp32 vectors: returns (out, exact64) where out is
+    R x count, every row the fp32 sum in rank order, and exact64 the fp64 sum."""
+    bufs, n, ptrs = _f32_list(bufs)
+    out = np.empty((len(bufs), n), np.float32)
+    ex = np.empty(n, np.float64)
+    rc = _load().oracle_allreduce_f32(ptrs, len(bufs), n, out.ctypes.data, ex.ctypes.data)
+    if rc:
+        raise ValueError(f"oracle_allreduce_f32 rc={rc}")
+    return out, ex
+
+
+def reduce_scatter(bufs, out=None):
+    """Reduce-scatter of R fp32 vectors into an R x count array: row r gets
+    chunk r of the rank-order fp32 sum; other positions keep `out`'s values."""
+    bufs, n, ptrs = _f32_list(bufs)
+    if out is None:
+        out = np.zeros((len(bufs), n), np.float32)
+    out = np.ascontiguousarray(out, np.float32)
+    rc = _load().oracle_reduce_scatter_f32(ptrs, len(bufs), n, out.ctypes.data)
+    if rc:
+        raise ValueError(f"oracle_reduce_scatter_f32 rc={rc}")
     return out
 
 

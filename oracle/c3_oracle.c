@@ -7,7 +7,9 @@
  * this file includes nothing from the CUDA side.
  *
  * What it computes, each function written straight from its definition, in
- * plain loops, fp64 for all floating point, no blocking and no reordering:
+ * plain loops, no blocking and no reordering, fp64 for all floating point
+ * except the all-reduce, whose definition here is the method's own fp32
+ * rank-order sum (returned beside the fp64 sum):
  *
  *   oracle_gemm / oracle_gemm_entries
  *       C[m][n] = sum_k A[m][k] * B[n][k]   (B stored N x K, the weight layout
@@ -27,6 +29,15 @@
  *       out[(j*R + i)*B + b] = in[(i*R + j)*B + b]: block j of rank i lands in
  *       slot i of rank j (the all-to-all collective named beside all-gather in
  *       the same pages; the block layout is this library's reading).
+ *
+ *   oracle_allreduce_f32 / oracle_reduce_scatter_f32
+ *       The all-reduce the pages decompose into a reduce-scatter (which needs
+ *       arithmetic, so it stays on compute units) and an all-gather (which a
+ *       DMA engine can carry) (synthesis page, "Attack 1"; pith.science paper
+ *       page, "Reading between the lines").  Every rank r ends with
+ *       out_r[i] = sum over q = 0..R-1, in increasing q, of in_q[i], summed in
+ *       fp32 (the precision this library's kernel uses; the pages fix none).
+ *       The fp64 sum is returned beside it for the rounding-error check.
  *
  *   oracle_c3_metrics
  *       ideal speedup = (T_gemm + T_comm) / max(T_gemm, T_comm) from isolated
@@ -166,6 +177,43 @@ int oracle_alltoall(const uint8_t *in, int nranks, int64_t block_bytes, uint8_t 
         for (int64_t j = 0; j < R; ++j)     /* destination rank */
             for (int64_t b = 0; b < block_bytes; ++b)
                 out[(j * R + i) * block_bytes + b] = in[(i * R + j) * block_bytes + b];
+    return 0;
+}
+
+/* All-reduce of R fp32 vectors of `count` elements: out[r*count + i] holds
+ * the fp32 sum over q of in[q][i], q increasing (identical on every rank r);
+ * exact64[i] (may be NULL) the same sum in fp64. */
+int oracle_allreduce_f32(const float *const *in, int nranks, int64_t count, float *out, double *exact64)
+{
+    if (nranks < 1 || count < 0 || !in || !out) return -1;
+    for (int q = 0; q < nranks; ++q)
+        if (!in[q] && count > 0) return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        float acc = 0.0f;
+        double acc64 = 0.0;
+        for (int q = 0; q < nranks; ++q) {
+            acc = acc + in[q][i];
+            acc64 += (double)in[q][i];
+        }
+        for (int r = 0; r < nranks; ++r) out[(int64_t)r * count + i] = acc;
+        if (exact64) exact64[i] = acc64;
+    }
+    return 0;
+}
+
+/* Reduce-scatter: rank r keeps only chunk r (count / R elements, at its own
+ * offset r * count / R) of the reduced vector; out is R * count floats and
+ * positions outside a rank's own chunk are left untouched. */
+int oracle_reduce_scatter_f32(const float *const *in, int nranks, int64_t count, float *out)
+{
+    if (nranks < 1 || count < 0 || !in || !out || count % nranks) return -1;
+    const int64_t chunk = count / nranks;
+    for (int r = 0; r < nranks; ++r)
+        for (int64_t i = r * chunk; i < (r + 1) * chunk; ++i) {
+            float acc = 0.0f;
+            for (int q = 0; q < nranks; ++q) acc = acc + in[q][i];
+            out[(int64_t)r * count + i] = acc;
+        }
     return 0;
 }
 

@@ -95,6 +95,12 @@ def test_argument_errors_before_any_cuda_call(c3):
     assert c3.c3_alltoall(0x10000, 0x10400, 32, 8, check=False) == c3.C3_EINVAL        # in/out overlap
     assert c3.c3_alltoall(0x10000, 0x20000, 40, 8, check=False) == c3.C3_EALIGN
     assert c3.c3_alltoall(0x10000, 0x20000, 0, 8, check=False) == c3.C3_OK
+    ins = [0x10000 * (r + 1) for r in range(8)]
+    assert c3.c3_allreduce(ins, 0x200000, 33, 8, check=False) == c3.C3_EALIGN        # count % 32
+    assert c3.c3_allreduce(ins, 0x200000, 64, 9, check=False) == c3.C3_EINVAL        # > 8 ranks
+    assert c3.c3_allreduce(ins, 0x10000, 64, 8, check=False) == c3.C3_EINVAL         # out overlaps input 0
+    assert c3.c3_allreduce(ins[:1] + [0x20004] + ins[2:], 0x200000, 64, 8, check=False) == c3.C3_EALIGN
+    assert c3.c3_allreduce(ins, 0x200000, 0, 8, check=False) == c3.C3_OK
     assert c3.c3_gemm_noalloc(0x1000, 0x1000, 0x1000, -1, 4, 8, check=False) == c3.C3_EINVAL
     assert c3.c3_gemm_noalloc(0x1000, 0x1000, 0x1000, 4, 4, 12, check=False) == c3.C3_EALIGN
     assert c3.c3_gemm_noalloc(None, None, None, 4, 0, 8, check=False) == c3.C3_OK

@@ -208,3 +208,50 @@ def test_copy_engine_variants_bit_exact(c3, variant, coll, unit):
         out.fill_(0x33)
         c3.c3_run(p, c3.C3_MODE_SERIAL_CE, 0, 0)
         assert np.array_equal(out.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------- all-reduce
+
+def _ar_check(out_dev, bufs):
+    ref, ex = oracle.allreduce(bufs)
+    got = out_dev.cpu().numpy().reshape(ref.shape)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), "differs from the rank-order fp32 sum"
+    # and the rank-order fp32 sum is within the sequential-summation bound of the exact sum
+    R = len(bufs)
+    bound = R * 2.0 ** -24 * np.sum(np.abs(np.stack(bufs).astype(np.float64)), axis=0)
+    assert (np.abs(ref[0].astype(np.float64) - ex) <= bound + 1e-45).all()
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("nranks,count", [(8, 1 << 18), (8, 32 * 37), (2, 8), (5, 20 * 9), (1, 4)])
+def test_allreduce_bit_exact(c3, engine, nranks, count):
+    bufs = [I.normal(1002 + r, count).astype(np.float32) for r in range(nranks)]
+    bufs[0][:3] = [-0.0, np.inf, 1e38]            # signed zero, infinity, overflow to inf in the sum
+    if nranks > 1:
+        bufs[1][2] = 1e38
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    out = torch.full((nranks * count,), float("nan"), dtype=torch.float32, device="cuda")
+    c3.c3_allreduce(dins, out, count, nranks, engine=engine)
+    c3.c3_status_check()
+    ref, _ = oracle.allreduce(bufs)
+    got = out.cpu().numpy().reshape(ref.shape)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("mode,split,prio", [(1, 0, 0), (1, 0, 1), (1, 16, 0), (2, 0, 0), (2, 8, 0), (0, 0, 0), (3, 0, 0)])
+@pytest.mark.parametrize("variant", [0, 2])
+def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
+    w = I.WORKLOADS["tiny_ar"]
+    A, B = I.gemm_operands(w)
+    bufs = I.coll_payload(w)
+    C_ref, S_ref = oracle.gemm(A, B)
+    dA, dB = dev_u16(A), dev_u16(B)
+    dC = torch.full((w.M, w.N), float("nan"), device="cuda")
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    out = torch.full((w.coll_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLREDUCE, out, w.unit_bytes, w.nranks, shards=dins,
+                   ce_variant=variant)
+    t = c3.c3_run(p, mode, split, prio)
+    assert t["status"] == 0
+    _ar_check(out, bufs)
+    assert_gemm_close(dC.cpu().numpy(), C_ref, S_ref)

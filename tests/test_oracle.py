@@ -281,3 +281,53 @@ def test_distributions_have_the_stated_moments():
     assert -1.0 <= u.min() and u.max() <= 1.0 and abs(u.mean()) < 0.01
     z = I.bf16_bits_to_f32(I.bf16_normal(1001, (1 << 16,), 0.0, 0.02))
     assert abs(z.std() - 0.02) < 0.001 and abs(z.mean()) < 0.001
+
+
+# ---------------------------------------------------------------- all-reduce pins
+
+def test_allreduce_integer_sums_exact_and_replicated():
+    R, n = 8, 40
+    bufs = [np.arange(n, dtype=np.float32) * (q + 1) - q for q in range(R)]
+    out, ex = oracle.allreduce(bufs)
+    # closed form: sum_q (i*(q+1) - q) = i*R(R+1)/2 - R(R-1)/2
+    expect = np.arange(n) * (R * (R + 1) // 2) - R * (R - 1) // 2
+    assert out.shape == (R, n)
+    for r in range(R):
+        assert np.array_equal(out[r], expect.astype(np.float32))
+    assert np.array_equal(ex, expect.astype(np.float64))
+
+
+def test_allreduce_rank_order_is_the_fp32_order():
+    # 1e8 + 1 + 1 - 1e8 ... : order matters in fp32; the rank order fixes it
+    bufs = [np.array([1e8], np.float32), np.array([1.0], np.float32), np.array([1.0], np.float32),
+            np.array([-1e8], np.float32)]
+    out, ex = oracle.allreduce(bufs)
+    f = np.float32(0)
+    for b in bufs:
+        f = np.float32(f + b[0])
+    assert out[0, 0] == f == np.float32(0.0)       # 1e8+1 rounds to 1e8 in fp32, twice
+    assert ex[0] == 2.0
+
+
+def test_allreduce_one_rank_is_identity_and_one_hot():
+    x = I.normal(3, 17).astype(np.float32)
+    out, _ = oracle.allreduce([x])
+    assert np.array_equal(out[0], x)
+    R, n = 4, 8
+    bufs = [np.zeros(n, np.float32) for _ in range(R)]
+    for q in range(R):
+        bufs[q][2 * q] = q + 1.5
+    out, _ = oracle.allreduce(bufs)
+    assert np.array_equal(out[1], np.array([1.5, 0, 2.5, 0, 3.5, 0, 4.5, 0], np.float32))
+
+
+def test_reduce_scatter_keeps_only_own_chunk():
+    R, n = 4, 12
+    bufs = [np.full(n, q + 1, np.float32) for q in range(R)]
+    out = oracle.reduce_scatter(bufs, np.full((R, n), -7.0, np.float32))
+    for r in range(R):
+        own = slice(r * 3, (r + 1) * 3)
+        assert np.array_equal(out[r, own], np.full(3, 10.0, np.float32))   # 1+2+3+4
+        mask = np.ones(n, bool)
+        mask[own] = False
+        assert np.all(out[r, mask] == -7.0)
