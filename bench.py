@@ -64,7 +64,7 @@ MODES = [
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=12)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -391,7 +391,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     dA = torch.from_numpy(A_h.view(np.int16)).to(dev)
     dB = torch.from_numpy(B_h.view(np.int16)).to(dev)
     dC = torch.empty((w0.M, w0.N), dtype=torch.float32, device=dev)
-    flush = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     for w in ws:
         payload = I.coll_payload(w)
@@ -441,7 +441,7 @@ def run_heuristics(args, c3, torch, np, I, dev, info):
     S = info["sm_count"]
     ks = [8, 16, 32, 64]
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
 
@@ -565,7 +565,7 @@ def main(argv=None):
     else:
         dshards, dsend, coll_id = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
     out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
-    flush = torch.empty(max(2 * info["l2_bytes"], 256 << 20), dtype=torch.uint8, device=dev)
+    flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
                       send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
@@ -673,7 +673,8 @@ def main(argv=None):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.description}", "M": w.M, "N": w.N, "K": w.K,
                    "collective": f"{w.coll} {w.nranks} ranks x {w.unit_bytes} B",
-                   "l2": f"flushed before every timed phase ({flush.numel() >> 20} MiB zero-fill)",
+                   "l2": f"flushed before every timed phase ({flush.numel() >> 20} MiB zero-fill, then its first "
+                         f"half read back so L2 holds clean lines)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "coll_l2": args.coll_l2, "ce_variant": args.ce_variant,
                    "modes": [m[0] for m in modes]},
@@ -730,7 +731,7 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
     (the pages' Figure 5b/c question: how many compute units a collective
     needs)."""
     res = {"gemm": {}, "copy_gbs_by_sms": {}}
-    flush_buf = torch.empty(2 * info["l2_bytes"], dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     do_flush = lambda: c3.c3_l2_flush(flush_buf, flush_buf.numel(), stream)  # noqa: E731
     g = torch.Generator(device=dev)
     g.manual_seed(1234)

@@ -124,5 +124,6 @@ void ce_release_graphs(int device);
 int status_reset_launch(DevStatus* st, cudaStream_t s);
 int selftest_wait_launch(DevStatus* st, unsigned long long limit_ns, int arrive, cudaStream_t s);
 int zero_fill_launch(void* buf, size_t bytes, cudaStream_t s);
+int l2_flush_launch(void* buf, size_t bytes, cudaStream_t s);
 
 }  // namespace c3

@@ -414,7 +414,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
 template <class F>
 static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, double* t_out, F fn) {
     int rc;
-    if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
+    if (p->flush_buf && p->flush_bytes && (rc = l2_flush_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
     cudaError_t e;
     if ((e = cudaEventRecord(ds.ev[4], s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     if ((rc = fn())) return rc;
@@ -587,7 +587,7 @@ int c3_allreduce(const float* const* inputs, float* out, size_t count, int nrank
 int c3_l2_flush(void* buf, size_t bytes, c3_stream s) {
     if (!buf && bytes) return set_error(C3_EINVAL, "buf is NULL");
     if (!aligned16(buf)) return set_error(C3_EALIGN, "buf must be 16-byte aligned");
-    return zero_fill_launch(buf, bytes, static_cast<cudaStream_t>(s));
+    return l2_flush_launch(buf, bytes, static_cast<cudaStream_t>(s));
 }
 
 int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing* out) {
@@ -638,7 +638,7 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
             return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
-        if (p->flush_buf && p->flush_bytes && (rc = zero_fill_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
+        if (p->flush_buf && p->flush_bytes && (rc = l2_flush_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
         r.mode = mode;
         r.sm_split = sm_split;
         r.priority = priority;

@@ -69,6 +69,39 @@ int selftest_wait_launch(DevStatus* st, unsigned long long limit_ns, int arrive,
     return 0;
 }
 
+// Reads `bytes` (16-byte loads cached in L2 only) without storing anything
+// unless the data would hold a pattern zero-filled memory cannot hold: after a
+// zero fill of a buffer twice the size of L2, reading its first half evicts
+// the dirty lines of its second half, so the next timed kernel starts with L2
+// holding clean lines and pays no write-back of the flush.
+__global__ void l2_clean_read_kernel(const uint8_t* buf, size_t bytes, uint32_t* sink) {
+    const size_t nvec = bytes >> 4;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    uint32_t acc = 0;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        uint4 v = __ldcg(reinterpret_cast<const uint4*>(buf) + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == 0x9E3779B9u) *sink = acc;
+}
+
+int l2_flush_launch(void* buf, size_t bytes, cudaStream_t s) {
+    int rc = zero_fill_launch(buf, bytes, s);
+    if (rc) return rc;
+    DeviceState* ds = device_state();
+    if (!ds) return -3;
+    const size_t half = (bytes / 2) & ~(size_t)15;
+    if (half == 0) return 0;
+    size_t want = ((half >> 4) + 255) / 256;
+    int grid = (int)(want < (size_t)ds->sm_count * 4 ? (want ? want : 1) : (size_t)ds->sm_count * 4);
+    l2_clean_read_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(buf), half,
+                                              reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(buf) + half));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_cuda_error(e, "L2 clean-read launch");
+    count_launch();
+    return 0;
+}
+
 int status_reset_launch(DevStatus* st, cudaStream_t s) {
     status_reset_kernel<<<1, kCtaRecs, 0, s>>>(st);
     cudaError_t e = cudaGetLastError();

@@ -215,8 +215,8 @@ typedef struct {
     int sm_kernel;             /* c3_sm_kernel */
     int coll_l2;               /* c3_l2_policy of the SM collective */
     int ce_variant;            /* c3_ce_variant of the copy-engine collective */
-    /* optional L2 flush between the phases of c3_time (caller-owned scratch,
-     * larger than L2; NULL = no flush) */
+    /* optional L2 flush (c3_l2_flush) before each phase of c3_time
+     * (caller-owned scratch, at least 2 x L2; NULL = no flush) */
     void *flush_buf;
     size_t flush_bytes;
     c3_stream stream;          /* runs fork from and join back to this stream */
@@ -361,8 +361,11 @@ int c3_rp_predict(const c3_rp_table *t, double gemm_flops, double gemm_bytes, do
                   double peak_flops, double peak_bytes_per_s, int *best_sms, double *t_pred_best,
                   double *t_pred_each);
 
-/* Writes `bytes` of zeros over `buf` (device) with an SM kernel: the L2 flush
- * used between timed phases.  Asynchronous on `s`. */
+/* The L2 flush used between timed phases: writes `bytes` of zeros over `buf`
+ * (device), then reads back its first half, so that L2 ends up holding clean
+ * lines (a write-only flush would leave L2 full of dirty lines whose
+ * write-back the next timed kernel pays for).  A complete flush needs
+ * bytes >= 2 x L2.  Two SM kernels, asynchronous on `s`. */
 int c3_l2_flush(void *buf, size_t bytes, c3_stream s);
 
 #ifdef __cplusplus
