@@ -46,7 +46,8 @@ UNIT = "% of ideal C3 gain"
 WORKLOAD = "mem_ag"
 
 # (name, mode, sm_split, priority).  Pages' names: c3_base, c3_sp, c3_rp (best
-# power-of-two split, oracle-selected), sp+rp, ConCCL, ConCCL_rp.
+# power-of-two split, oracle-selected), sp+rp, ConCCL, ConCCL_rp; reclaim_k is
+# this library's SM partition that lasts only as long as the collective.
 MODES = [
     ("baseline", 1, 0, 0),
     ("prioritised", 1, 0, 1),
@@ -55,6 +56,8 @@ MODES = [
     ("partitioned_32", 1, 32, 0),
     ("partitioned_64", 1, 64, 0),
     ("prio_partitioned_32", 1, 32, 1),
+    ("reclaim_16", 4, 16, 0),
+    ("reclaim_32", 4, 32, 0),
     ("ce", 2, 0, 0),
     ("ce_rp_8", 2, 8, 0),
     ("ce_rp_16", 2, 16, 0),
@@ -383,7 +386,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     """The pages' size sweep: an 8192^3 GEMM against collectives of 1 MiB to
     1 GiB total (x2 steps), every mode of --modes (default: baseline,
     prioritised, partitioned_32, ce), one JSON line per size."""
-    names = args.modes.split(",") if args.modes else ["baseline", "prioritised", "partitioned_32", "ce"]
+    names = args.modes.split(",") if args.modes else ["baseline", "prioritised", "partitioned_32", "reclaim_16", "ce"]
     modes = [m for m in MODES if m[0] in names]
     ws = I.sweep_workloads(args.sweep)
     w0 = ws[0]

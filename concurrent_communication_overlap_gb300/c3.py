@@ -19,6 +19,7 @@ C3_OK, C3_EINVAL, C3_EALIGN, C3_ECUDA, C3_ETIMEOUT, C3_EUNSUP = 0, -1, -2, -3, -
 C3_ENGINE_SM, C3_ENGINE_CE = 0, 1
 C3_COLL_ALLGATHER, C3_COLL_ALLTOALL, C3_COLL_ALLREDUCE = 0, 1, 2
 C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_CE = 0, 1, 2, 3
+C3_MODE_CONCURRENT_SM_RECLAIM = 4
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
 C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH = 0, 1, 2

@@ -16,6 +16,7 @@ struct CtaRec {
 };
 
 constexpr int kCtaRecs = 256;      // CTAs recorded per kernel (the first 256)
+constexpr int kSchedSlots = 64;    // GEMM tile-scheduler counters, used round-robin by launches
 
 // Device status block (library-owned, reset before each timed run).
 struct DevStatus {
@@ -30,6 +31,12 @@ struct DevStatus {
     unsigned int smid_comm[8];     // bitmap of SMs that ran a collective CTA
     CtaRec gemm_rec[kCtaRecs];     // per-CTA residency, indexed by blockIdx.x
     CtaRec comm_rec[kCtaRecs];
+    // Dynamic tile scheduler of the persistent GEMM: per slot, the next tile
+    // to hand out and the number of CTAs done.  A launch takes one slot; its
+    // last CTA puts both back to zero.  Zeroed when the block is created;
+    // the per-run reset leaves them alone (a GEMM of another stream may be
+    // using a slot).
+    unsigned int sched[kSchedSlots][2];
 };
 
 constexpr size_t kStatusBytes = 16384;
@@ -90,6 +97,7 @@ struct DeviceState {
     cudaStream_t s_capture = nullptr;  // private stream for capturing copy-engine graphs
     cudaEvent_t ev[8] = {};
     DevStatus* status = nullptr;       // device status block
+    unsigned int next_sched = 0;       // round-robin scheduler slot
     bool ready = false;
 };
 
@@ -107,6 +115,7 @@ int set_error(int code, const char* what);
 // Kernels' host launchers.  Return 0 or a negative c3_status.
 int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
                 int sm_budget, cudaStream_t s, DevStatus* st, int* ctas_out);
+void gemm_sched_reset(DevStatus* st);  // zero every scheduler slot (host; after an aborted launch)
 int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, int* grid);
 int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration
 int gemm_init_device();  // function attributes; once per device

@@ -321,6 +321,8 @@ static int read_status(DeviceState& ds, c3_timing* out) {
         out->smid_overlap = coresident_sms(h, &out->sms_shared_any);
     }
     if (h.error) {
+        // a launch that gave up may have left its tile-scheduler slot non-zero
+        gemm_sched_reset(ds.status);
         char buf[128];
         std::snprintf(buf, sizeof buf, "device wait gave up (site %d)", h.where);
         return set_error(h.error, buf);
@@ -383,12 +385,16 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         cudaStream_t sc = priority ? ds.s_comm_hi : ds.s_comm;
         if ((e = cudaStreamWaitEvent(sg, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
-        const int gemm_budget = sm_split > 0 ? ds.sm_count - sm_split : 0;
+        const bool reclaim = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
+        if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
+        // reclaim: the GEMM is launched on every SM and its CTAs that find no
+        // free SM start when the collective's SMs free up
+        const int gemm_budget = (sm_split > 0 && !reclaim) ? ds.sm_count - sm_split : 0;
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
         auto go_gemm = [&] { return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, gemm_budget, sg, ds.status, &gctas); };
         auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas); };
-        if (priority) {
+        if (priority || reclaim) {
             if ((rc = go_comm())) return rc;
             if ((rc = go_gemm())) return rc;
         } else {
@@ -593,7 +599,7 @@ int c3_l2_flush(void* buf, size_t bytes, c3_stream s) {
 int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing* out) {
     if (!out) return set_error(C3_EINVAL, "out is NULL");
     std::memset(out, 0, sizeof *out);
-    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
+    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_CONCURRENT_SM_RECLAIM) return set_error(C3_EINVAL, "unknown mode");
     if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
     CollPlan t;
     int rc = check_problem(p, &t);
@@ -612,7 +618,7 @@ int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing*
 int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmup, int reps,
             c3_timing* per_rep) {
     if (!per_rep || reps < 1 || warmup < 0) return set_error(C3_EINVAL, "need reps >= 1, warmup >= 0, per_rep");
-    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_SERIAL_CE) return set_error(C3_EINVAL, "unknown mode");
+    if (mode < C3_MODE_SERIAL_SM || mode > C3_MODE_CONCURRENT_SM_RECLAIM) return set_error(C3_EINVAL, "unknown mode");
     if (priority != 0 && priority != 1) return set_error(C3_EINVAL, "priority must be 0 or 1");
     CollPlan t;
     int rc = check_problem(p, &t);

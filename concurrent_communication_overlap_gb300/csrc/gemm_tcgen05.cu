@@ -17,9 +17,11 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, fp32 stores to C
 //               with edge masking, then release the accumulator.
 // The two accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.  Tiles are dealt round-robin (tile = blockIdx.x + i * gridDim.x)
-// in a grouped order: GROUP_M row blocks advance together so that the CTAs
-// in flight share A row blocks and B column blocks in L2.
+// tile i+1.  Tiles are claimed one by one from an atomic counter (a
+// scheduler slot in the status block), in a grouped order: GROUP_M row blocks
+// advance together so that the tiles in flight share A row blocks and B
+// column blocks in L2.  A CTA slowed by a neighbour, or started late because
+// its SM was held by a collective, claims fewer tiles.
 #include "c3_device.cuh"
 #include "c3_internal.h"
 
@@ -91,7 +93,7 @@ template <int BN, int MSUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      float* __restrict__ C, int M, int N, int num_m, int num_n, int num_kb,
-                     DevStatus* st) {
+                     unsigned int* sched, DevStatus* st) {
     using Cfg = GemmCfg<BN, MSUB>;
     constexpr int S = Cfg::kStages;
     constexpr int NB = Cfg::kAccBufs;
@@ -102,13 +104,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     // ring: stage i = [A sub-tile 0 .. MSUB-1][B], then barriers
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * Cfg::kStageBytes);
-    // bars[0..S) full, [S..2S) empty, [2S..2S+NB) tmem_full, [2S+NB..2S+2NB) tmem_empty, [2S+2NB] drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NB + 1);
+    // bars[0..S) full, [S..2S) empty, [2S..2S+NB) tmem_full, [2S+NB..2S+2NB) tmem_empty, [2S+2NB] drain,
+    // then the tile ring's full and empty barriers
+    constexpr int kTR = 4;  // tile-id ring between the producer and the MMA / epilogue roles
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NB + 1 + 2 * kTR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     auto stage_a = [&](int stage, int sub) { return base + (uint32_t)stage * Cfg::kStageBytes + (uint32_t)sub * Cfg::kABytes; };
     auto stage_b = [&](int stage) { return base + (uint32_t)stage * Cfg::kStageBytes + MSUB * Cfg::kABytes; };
     const int BAR_TFULL = 2 * S, BAR_TEMPTY = 2 * S + NB, BAR_DRAIN = 2 * S + 2 * NB;
+    const int BAR_RFULL = BAR_DRAIN + 1, BAR_REMPTY = BAR_RFULL + kTR;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -126,6 +132,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(bar(BAR_TEMPTY + b), 4 * 32);
         }
         mbar_init(bar(BAR_DRAIN), 1);
+        for (int i = 0; i < kTR; ++i) {
+            mbar_init(bar(BAR_RFULL + i), 1);
+            mbar_init(bar(BAR_REMPTY + i), 1 + 4);  // the MMA thread + one arrival per epilogue warp
+        }
         fence_barrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -141,15 +151,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer
+            // ---------------- TMA producer (and tile scheduler)
+            // Tiles are claimed one at a time from the launch's counter (or
+            // dealt round-robin when there is none), published to the other
+            // roles through the tile ring, and the sentinel total_tiles ends
+            // every role's loop.  A CTA that starts late (its SM was busy)
+            // simply claims fewer tiles.
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b = policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            int t = sched ? (int)min(atomicAdd(&sched[0], 1u), (unsigned)total_tiles) : (int)blockIdx.x;
+            for (int i = 0;; ++i) {
+                const int slot = i & (kTR - 1);
+                if (!mbar_wait(bar(BAR_REMPTY + slot), ((uint32_t)(i / kTR) & 1u) ^ 1u, abort_flag)) {
+                    report_error(st, -4, kSiteGemmProducer);
+                    break;
+                }
+                tile_ring[slot] = t < total_tiles ? t : total_tiles;
+                mbar_arrive(bar(BAR_RFULL + slot));
+                if (t >= total_tiles) break;
+                const int next =
+                    sched ? (int)min(atomicAdd(&sched[0], 1u), (unsigned)total_tiles) : t + (int)gridDim.x;
                 int mb, nb;
                 tile_coords(t, num_m, num_n, mb, nb);
+                bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(bar(S + stage), phase ^ 1u, abort_flag)) {
                         report_error(st, -4, kSiteGemmProducer);
@@ -166,6 +192,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
+                t = next;
+            }
+            // The launch's last CTA to finish puts its scheduler slot back to zero.
+            if (sched) {
+                __threadfence();
+                if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+                    atomicExch(&sched[0], 0u);
+                    atomicExch(&sched[1], 0u);
+                }
             }
             // Drain: the last load issued into each stage must have landed before
             // the CTA exits (a no-op when the MMA warp consumed everything).  The
@@ -177,7 +213,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!mbar_wait(bar(i), (i < stage) ? phase : (phase ^ 1u), &no_abort))
                     report_error(st, -4, kSiteGemmDrain);
             }
-            (void)ok;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -185,9 +220,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t idesc = make_idesc<BN>();
             int stage = 0;
             uint32_t phase = 0;
-            int local = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++local) {
+            for (int local = 0; ok; ++local) {
+                const int slot = local & (kTR - 1);
+                if (!mbar_wait(bar(BAR_RFULL + slot), (uint32_t)(local / kTR) & 1u, abort_flag)) {
+                    report_error(st, -4, kSiteGemmMma);
+                    break;
+                }
+                const int t = tile_ring[slot];
+                mbar_arrive(bar(BAR_REMPTY + slot));
+                if (t >= total_tiles) break;
                 const int buf = local % NB;
                 const uint32_t use = (uint32_t)(local / NB);
                 if (!mbar_wait(bar(BAR_TEMPTY + buf), (use & 1u) ^ 1u, abort_flag)) {
@@ -232,8 +274,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------- epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
         const int q = warp & 3;
         const bool vec_ok = (N & 3) == 0;
-        int local = 0;
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++local) {
+        for (int local = 0;; ++local) {
+            const int slot = local & (kTR - 1);
+            const bool have = mbar_wait(bar(BAR_RFULL + slot), (uint32_t)(local / kTR) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, have)) {
+                report_error(st, -4, kSiteGemmEpilogue);
+                break;
+            }
+            const int t = tile_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_REMPTY + slot));
+            if (t >= total_tiles) break;
             const int buf = local % NB;
             const uint32_t use = (uint32_t)(local / NB);
             // tcgen05.ld is warp-collective: the whole warp leaves together if
@@ -387,11 +438,11 @@ static int choose_cfg(int64_t M, int64_t N, int64_t K, int cap) {
 }
 
 static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, float* C, int64_t M, int64_t N,
-                      int64_t num_m, int64_t num_n, int num_kb, DevStatus* st, cudaStream_t s) {
+                      int64_t num_m, int64_t num_n, int num_kb, unsigned int* sched, DevStatus* st, cudaStream_t s) {
     const TileCfg& c = kCfgs[ci];
 #define C3_LAUNCH(BN_, MS_)                                                                                  \
     gemm_bf16_kernel<BN_, MS_><<<grid, kGemmThreads, GemmCfg<BN_, MS_>::kSmem, s>>>(                           \
-        ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, st)
+        ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, sched, st)
     if (c.bn == 256 && c.msub == 1) C3_LAUNCH(256, 1);
     else if (c.bn == 128 && c.msub == 1) C3_LAUNCH(128, 1);
     else if (c.bn == 256 && c.msub == 2) C3_LAUNCH(256, 2);
@@ -436,10 +487,15 @@ int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, in
     GemmPlan p;
     int rc = plan_gemm(A, B, M, N, K, cap, &p);
     if (rc) return rc;
-    rc = launch_cfg(p.ci, p.grid, p.ma, p.mb, C, M, N, p.num_m, p.num_n, p.num_kb, st, s);
+    unsigned int* sched = st ? st->sched[ds->next_sched++ % kSchedSlots] : nullptr;
+    rc = launch_cfg(p.ci, p.grid, p.ma, p.mb, C, M, N, p.num_m, p.num_n, p.num_kb, sched, st, s);
     if (rc) return rc;
     if (ctas_out) *ctas_out = p.grid;
     return 0;
+}
+
+void gemm_sched_reset(DevStatus* st) {
+    if (st) cudaMemset(st->sched, 0, sizeof st->sched);
 }
 
 int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, int* grid) {
@@ -470,6 +526,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kStatusBytes];
 struct NoAllocDevice {
     bool ready = false;
     int sm_count = 0;
+    unsigned int next_sched = 0;
     DevStatus* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
 static NoAllocDevice g_noalloc[64];
@@ -534,8 +591,9 @@ extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M
         return set_error(-5, "c3_gemm_noalloc: more than 256 CTAs would need more than its 16 KiB scratch");
     // The block keeps the previous call's contents: clear it on this stream first.
     if ((rc = status_reset_launch(d->scratch, s))) return rc;
+    unsigned int* sched = d->scratch->sched[d->next_sched++ % kSchedSlots];
     if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, C, M, N, plan.num_m, plan.num_n, plan.num_kb,
-                         d->scratch, s)))
+                         sched, d->scratch, s)))
         return rc;
     cudaError_t e;
     if (!check) return 0;

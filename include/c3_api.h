@@ -65,7 +65,8 @@ typedef enum {
     C3_MODE_SERIAL_SM = 0,     /* GEMM, then the collective on SMs, one stream */
     C3_MODE_CONCURRENT_SM = 1, /* GEMM || collective on SMs (baseline / prioritised / partitioned) */
     C3_MODE_CONCURRENT_CE = 2, /* GEMM || collective on copy engines (ConCCL, ConCCL_rp) */
-    C3_MODE_SERIAL_CE = 3      /* GEMM, then the collective on copy engines, one stream */
+    C3_MODE_SERIAL_CE = 3,     /* GEMM, then the collective on copy engines, one stream */
+    C3_MODE_CONCURRENT_SM_RECLAIM = 4 /* SM partitioning with reclaim (see c3_run) */
 } c3_mode;
 
 /* SM copy kernel flavour.  VEC: 16-byte vector loads/stores, no shared memory,
@@ -131,7 +132,9 @@ uint64_t c3_kernel_launches(void);
  *      (the TMA row pitch must be a multiple of 16 bytes; else C3_EALIGN);
  *      K == 0 writes zeros.  M*N == 0 launches nothing.
  *   sm_budget  number of persistent CTAs, one per SM (0 = every SM); values
- *      above the SM count are clamped.
+ *      above the SM count are clamped.  The CTAs claim output tiles one at a
+ *      time from a counter in the library's status block, so a CTA that is
+ *      slowed or starts late does less of the work.
  * bf16 products are accumulated in fp32 on the tensor cores (tcgen05).
  * Asynchronous on `s`.
  */
@@ -265,6 +268,13 @@ typedef struct {
  *   mode C3_MODE_CONCURRENT_CE: the collective as copy-engine transfers on its
  *     own stream (ConCCL); sm_split > 0 removes that many SMs from the GEMM
  *     (ConCCL_rp).  priority as above.
+ *   mode C3_MODE_CONCURRENT_SM_RECLAIM (sm_split >= 1): SM partitioning with
+ *     reclaim -- the collective is launched first on sm_split SMs it holds
+ *     alone, the GEMM on every SM; the GEMM CTAs that find no free SM start
+ *     as soon as the collective's SMs free up and, since the GEMM claims its
+ *     tiles dynamically, take only the tiles still left.  The partition lasts
+ *     as long as the collective, not as long as the GEMM.  priority selects
+ *     the collective's stream priority.
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error

@@ -24,6 +24,8 @@ MODES = [  # (name, mode, sm_split, priority)
     ("ce", 2, 0, 0),
     ("ce_rp8", 2, 8, 0),
     ("serial_ce", 3, 0, 0),
+    ("reclaim16", 4, 16, 0),
+    ("reclaim32_prio", 4, 32, 1),
 ]
 
 
@@ -99,6 +101,32 @@ def test_partitioned_runs_on_disjoint_sms(c3, setup, split):
     assert t["comm_sms"] <= split
     assert t["gemm_ctas"] <= info["sm_count"] - split
     setup.verify()
+
+
+@pytest.mark.parametrize("split", [8, 32])
+def test_reclaim_never_shares_an_sm_at_once(c3, setup, split):
+    # the GEMM may reuse the collective's SMs after it leaves, never during
+    setup.poison()
+    t = c3.c3_run(setup.p, 4, split, 0)
+    assert t["smid_overlap"] == 0, t
+    assert t["comm_sms"] <= split
+    setup.verify()
+
+
+def test_scheduler_slots_recycle_over_many_launches(c3):
+    # more launches than scheduler slots (64): every slot must come back to zero
+    M, N, K = 640, 1000, 128          # 5 x 8 = 40 tiles of 128 x 128
+    A = I.bf16_uniform(5, (M, K))
+    B = I.bf16_uniform(6, (N, K))
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    C_ref, S_ref = oracle.gemm(A, B)
+    for i in range(150):
+        dC.fill_(float("nan"))
+        c3.c3_gemm(dA, dB, dC, M, N, K, 1 + i % 7)
+    c3.c3_status_check()
+    assert (np.abs(dC.cpu().numpy() - C_ref) <= TOL * S_ref).all()
 
 
 def test_ce_with_gemm_cap_leaves_sms_free(c3, setup):
