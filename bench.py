@@ -82,6 +82,10 @@ def parse_args(argv=None):
     ap.add_argument("--heuristics", action="store_true",
                     help="instead of the headline line: calibrate the SM-split slowdown table once, then compare the "
                          "split the pages' heuristic predicts with the swept best over the size sweep")
+    ap.add_argument("--profile-range", choices=["gemm", "baseline", "ce"], default=None,
+                    help="instead of the headline line: run one phase (the GEMM alone, or the GEMM concurrent with "
+                         "the SM collective / the copy engines) between cudaProfilerStart and cudaProfilerStop, for "
+                         "ncu --replay-mode app-range --profile-from-start off")
     ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
                     help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
     return ap.parse_args(argv)
@@ -573,6 +577,24 @@ def main(argv=None):
     prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
                       send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
                           ce_variant=ce_variant_arg(args, c3))
+
+    if args.profile_range:
+        # one profiled phase on the real workload buffers, after a few untimed runs
+        for _ in range(3):
+            c3.c3_run(prob, c3.C3_MODE_CONCURRENT_SM, 0, 0)
+            c3.c3_run(prob, c3.C3_MODE_CONCURRENT_CE, 0, 0)
+        c3.c3_l2_flush(flush, flush.numel(), stream)
+        torch.cuda.synchronize(dev)
+        torch.cuda.profiler.start()
+        if args.profile_range == "gemm":
+            c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
+            torch.cuda.synchronize(dev)
+        else:
+            c3.c3_run(prob, c3.C3_MODE_CONCURRENT_SM if args.profile_range == "baseline" else c3.C3_MODE_CONCURRENT_CE,
+                      0, 0)
+        torch.cuda.profiler.stop()
+        print(json.dumps({"profile_range": args.profile_range, "workload": w.name}), flush=True)
+        return 0
 
     # ---- warm-up steps
     for _ in range(args.warmup):

@@ -255,3 +255,47 @@ def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
     assert t["status"] == 0
     _ar_check(out, bufs)
     assert_gemm_close(dC.cpu().numpy(), C_ref, S_ref)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+@pytest.mark.parametrize("wname,rows", [("ffn70_ag", [0, 4095, 8191]), ("l405_a2a", [0, 8191])])
+def test_gemm_full_size_compute_bound_sampled(c3, wname, rows):
+    # the compute-bound workloads' GEMMs in the bench's launch configuration,
+    # checked on full rows (every tile column) and 256 random entries
+    w = I.WORKLOADS[wname]
+    assert c3.c3_gemm_plan(w.M, w.N, w.K, 0) == (256, 2, 152)
+    A, B = I.gemm_operands(w)
+    dA, dB = dev_u16(A), dev_u16(B)
+    dC = torch.full((w.M, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K)
+    c3.c3_status_check()
+    del dA, dB
+    rows = np.array(rows)
+    C_ref, S_ref = oracle.gemm(A[rows], B)
+    assert_gemm_close(dC[torch.from_numpy(rows).cuda()].cpu().numpy(), C_ref, S_ref)
+    rng = np.random.default_rng(11)
+    mi, ni = rng.integers(0, w.M, 256), rng.integers(0, w.N, 256)
+    c_ref, s_ref = oracle.gemm_entries(A, B, mi, ni)
+    got = dC[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()].cpu().numpy()
+    assert_gemm_close(got, c_ref, s_ref)
+
+
+@pytest.mark.parametrize("wname", ["ffn70_ag", "l405_a2a", "mem_ar"])
+@pytest.mark.parametrize("engine", [0, 1])
+def test_collective_full_size_bit_exact(c3, wname, engine):
+    w = I.WORKLOADS[wname]
+    payload = I.coll_payload(w)
+    out = torch.zeros(w.coll_bytes, dtype=torch.uint8, device="cuda")
+    if w.coll == "allgather":
+        c3.c3_allgather([dev_bytes(x) for x in payload], out, w.unit_bytes, w.nranks, engine=engine)
+        ref = oracle.allgather(payload)
+    elif w.coll == "alltoall":
+        c3.c3_alltoall(dev_bytes(payload), out, w.unit_bytes, w.nranks, engine=engine)
+        ref = oracle.alltoall(payload, w.nranks)
+    else:
+        c3.c3_allreduce([torch.from_numpy(x).cuda() for x in payload], out, w.unit_bytes // 4, w.nranks,
+                        engine=engine)
+        ref = oracle.allreduce(payload)[0].reshape(-1).view(np.uint8)
+    c3.c3_status_check()
+    assert np.array_equal(out.cpu().numpy(), ref)
