@@ -358,7 +358,10 @@ def run_reference(args, world, rank, pg):
         return 0
     w = I.WORKLOADS[args.workload]
     t0 = time.perf_counter()
-    recs, sample, cores = cpu_c3(w, args.steps, args.warmup, target_s=0.5)
+    # size the sample so that the whole run (3 oracle GEMM phases per step)
+    # stays near a minute, whatever --steps asks for
+    target = min(0.5, 60.0 / (3.0 * max(1, args.steps + args.warmup)))
+    recs, sample, cores = cpu_c3(w, args.steps, args.warmup, target_s=target)
     wall = time.perf_counter() - t0
     m, (tg, tc, tconc) = summarize_cpu(recs)
     value = m["pct_ideal_gain"]
