@@ -2,6 +2,7 @@
 // (host side).  Not installed; the public boundary is include/c3_api.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -115,6 +116,21 @@ int set_error(int code, const char* what);
 // Kernels' host launchers.  Return 0 or a negative c3_status.
 int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
                 int sm_budget, cudaStream_t s, DevStatus* st, int* ctas_out);
+
+// A GEMM planned on the host (tile configuration, grid, tensor maps), ready to
+// enqueue: the timed paths prepare before their start event so that host-side
+// planning is not counted as device time.
+struct GemmLaunch {
+    int kind = 0;  // 0: nothing to do, 1: zero fill (K == 0), 2: the kernel
+    float* C = nullptr;
+    int64_t M = 0, N = 0, K = 0;
+    int ci = 0, grid = 0, num_kb = 0;
+    int64_t num_m = 0, num_n = 0;
+    CUtensorMap ma, mb;
+};
+int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
+                 GemmLaunch* g);
+int gemm_enqueue(const GemmLaunch& g, cudaStream_t s, DevStatus* st, int* ctas_out);
 void gemm_sched_reset(DevStatus* st);  // zero every scheduler slot (host; after an aborted launch)
 int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, int* grid);
 int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration

@@ -370,9 +370,15 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     int gctas = 0, cctas = 0;
     const bool serial = (mode == C3_MODE_SERIAL_SM || mode == C3_MODE_SERIAL_CE);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
+    // Host-side GEMM planning (tile choice, tensor maps) happens before the
+    // start event: only device work and launch calls are timed.
+    const bool reclaim_mode = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
+    const int gemm_cap = (!serial && sm_split > 0 && !reclaim_mode) ? ds.sm_count - sm_split : 0;
+    GemmLaunch gl;
+    if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, gemm_cap, &gl))) return rc;
     if ((e = cudaEventRecord(ev0, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     if (serial) {
-        rc = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds.status, &gctas);
+        rc = gemm_enqueue(gl, s0, ds.status, &gctas);
         if (rc) return rc;
         if ((e = cudaEventRecord(ev_g, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
         rc = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, &cctas);
@@ -389,10 +395,9 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
         // reclaim: the GEMM is launched on every SM and its CTAs that find no
         // free SM start when the collective's SMs free up
-        const int gemm_budget = (sm_split > 0 && !reclaim) ? ds.sm_count - sm_split : 0;
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
-        auto go_gemm = [&] { return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, gemm_budget, sg, ds.status, &gctas); };
+        auto go_gemm = [&] { return gemm_enqueue(gl, sg, ds.status, &gctas); };
         auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas); };
         if (priority || reclaim) {
             if ((rc = go_comm())) return rc;
@@ -631,16 +636,16 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
     for (int it = 0; it < warmup + reps; ++it) {
         c3_timing r;
         std::memset(&r, 0, sizeof r);
-        rc = time_phase(*ds, s0, p, &r.t_gemm_iso, [&] {
-            return gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
-        });
+        GemmLaunch gl;
+        if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, 0, &gl))) return rc;
+        rc = time_phase(*ds, s0, p, &r.t_gemm_iso, [&] { return gemm_enqueue(gl, s0, ds->status, nullptr); });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_comm_iso, [&] {
             return launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
         rc = time_phase(*ds, s0, p, &r.t_serial_meas, [&] {
-            int r1 = gemm_launch(p->A, p->B, p->C, p->M, p->N, p->K, 0, s0, ds->status, nullptr);
+            int r1 = gemm_enqueue(gl, s0, ds->status, nullptr);
             return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;

@@ -476,22 +476,54 @@ static int plan_gemm(const void* A, const void* B, int64_t M, int64_t N, int64_t
     return make_map(&p->mb, B, N, K, c.bn);
 }
 
-int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
-                cudaStream_t s, DevStatus* st, int* ctas_out) {
-    if (ctas_out) *ctas_out = 0;
+int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
+                 GemmLaunch* g) {
+    g->kind = 0;
+    g->C = C;
+    g->M = M;
+    g->N = N;
+    g->K = K;
     if (M == 0 || N == 0) return 0;
-    if (K == 0) return zero_fill_launch(C, (size_t)M * (size_t)N * sizeof(float), s);
+    if (K == 0) {
+        g->kind = 1;
+        return 0;
+    }
     DeviceState* ds = device_state();
     if (!ds) return -3;
     const int cap = (sm_budget <= 0 || sm_budget > ds->sm_count) ? ds->sm_count : sm_budget;
     GemmPlan p;
     int rc = plan_gemm(A, B, M, N, K, cap, &p);
     if (rc) return rc;
-    unsigned int* sched = st ? st->sched[ds->next_sched++ % kSchedSlots] : nullptr;
-    rc = launch_cfg(p.ci, p.grid, p.ma, p.mb, C, M, N, p.num_m, p.num_n, p.num_kb, sched, st, s);
-    if (rc) return rc;
-    if (ctas_out) *ctas_out = p.grid;
+    g->kind = 2;
+    g->ci = p.ci;
+    g->grid = p.grid;
+    g->num_kb = p.num_kb;
+    g->num_m = p.num_m;
+    g->num_n = p.num_n;
+    g->ma = p.ma;
+    g->mb = p.mb;
     return 0;
+}
+
+int gemm_enqueue(const GemmLaunch& g, cudaStream_t s, DevStatus* st, int* ctas_out) {
+    if (ctas_out) *ctas_out = 0;
+    if (g.kind == 0) return 0;
+    if (g.kind == 1) return zero_fill_launch(g.C, (size_t)g.M * (size_t)g.N * sizeof(float), s);
+    DeviceState* ds = device_state();
+    if (!ds) return -3;
+    unsigned int* sched = st ? st->sched[ds->next_sched++ % kSchedSlots] : nullptr;
+    int rc = launch_cfg(g.ci, g.grid, g.ma, g.mb, g.C, g.M, g.N, g.num_m, g.num_n, g.num_kb, sched, st, s);
+    if (rc) return rc;
+    if (ctas_out) *ctas_out = g.grid;
+    return 0;
+}
+
+int gemm_launch(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
+                cudaStream_t s, DevStatus* st, int* ctas_out) {
+    GemmLaunch g;
+    int rc = gemm_prepare(A, B, C, M, N, K, sm_budget, &g);
+    if (rc) return rc;
+    return gemm_enqueue(g, s, st, ctas_out);
 }
 
 void gemm_sched_reset(DevStatus* st) {
