@@ -75,7 +75,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
     ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
-    ap.add_argument("--ce-variant", choices=["per_segment", "strided", "graph"], default="graph",
+    ap.add_argument("--ce-variant", choices=["per_segment", "strided", "graph", "graph_parallel"], default="graph",
                     help="how the copy-engine modes issue their transfers")
     ap.add_argument("--coll-l2", choices=["normal", "evict_first"], default="normal",
                     help="L2 policy of the SM collective's loads and stores")
@@ -393,7 +393,8 @@ def coll_l2_arg(args, c3):
 
 
 def ce_variant_arg(args, c3):
-    return {"per_segment": c3.C3_CE_PER_SEGMENT, "strided": c3.C3_CE_STRIDED, "graph": c3.C3_CE_GRAPH}[args.ce_variant]
+    return {"per_segment": c3.C3_CE_PER_SEGMENT, "strided": c3.C3_CE_STRIDED, "graph": c3.C3_CE_GRAPH,
+            "graph_parallel": c3.C3_CE_GRAPH_PARALLEL}[args.ce_variant]
 
 
 def run_sweep(args, c3, torch, np, I, dev, info):

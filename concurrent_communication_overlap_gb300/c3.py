@@ -22,7 +22,7 @@ C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_
 C3_MODE_CONCURRENT_SM_RECLAIM = 4
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
-C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH = 0, 1, 2
+C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH, C3_CE_GRAPH_PARALLEL = 0, 1, 2, 3
 CLASS_NAMES = {0: "G-long", 1: "GC-equal", 2: "C-long"}
 
 _i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t

@@ -72,7 +72,7 @@ struct SegTable {
     int pad;
 };
 
-enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2 };
+enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2, kCeGraphParallel = 3 };
 
 // A collective as launched: an optional reduce-scatter pass on SMs (all-reduce
 // only) followed by the segment copies on the chosen engine.

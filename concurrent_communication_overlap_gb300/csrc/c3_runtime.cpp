@@ -348,7 +348,8 @@ static int check_problem(const c3_problem* p, CollPlan* cp) {
     if (rc) return rc;
     if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
     if (p->coll_l2 != C3_L2_NORMAL && p->coll_l2 != C3_L2_EVICT_FIRST) return set_error(C3_EINVAL, "bad coll_l2");
-    if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH) return set_error(C3_EINVAL, "bad ce_variant");
+    if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH_PARALLEL)
+        return set_error(C3_EINVAL, "bad ce_variant");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
     if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
     const size_t cb = p->coll == C3_COLL_ALLREDUCE ? p->unit_bytes * (size_t)p->nranks

@@ -19,6 +19,12 @@
 //                rank (its R blocks land R blocks apart); all-gathers as above;
 //   GRAPH        the STRIDED calls captured once into a CUDA graph (cached by
 //                buffer addresses and size) and replayed with one launch.
+//   GRAPH_PARALLEL  a CUDA graph of independent copy nodes (strided 2-D nodes
+//                for the all-to-all, 1-D pieces otherwise): with no edges the
+//                driver spreads them over several copy engines.  Measured on
+//                GB300: as fast as the SM kernel alone for all-gathers of
+//                >= 128 MiB, but a concurrent GEMM runs much slower beside it,
+//                and so do later concurrent runs in the same process.  Opt-in.
 #include "c3_internal.h"
 
 #include <cstring>
@@ -50,6 +56,7 @@ static int ce_strided(const SegTable& t, cudaStream_t s) {
 // Small cache of instantiated graphs, keyed by the exact segment table.
 struct GraphEntry {
     bool used = false;
+    bool parallel = false;
     int device = -1;
     SegTable key;
     cudaGraphExec_t exec = nullptr;
@@ -66,13 +73,81 @@ static bool same_table(const SegTable& a, const SegTable& b) {
     return true;
 }
 
-static int ce_graph(const SegTable& t, cudaStream_t s, cudaStream_t capture_stream) {
+// Builds a graph directly, with no edges between the copy nodes, so that the
+// driver may run them on several copy engines at once (a stream-captured graph
+// would chain them in issue order).  The all-to-all uses one strided 2-D node
+// per source rank; other collectives one 1-D node per segment, each segment
+// cut into pieces of at least kPieceBytes when there is room (at most 64
+// nodes), to spread large transfers over more engines.
+constexpr uint64_t kPieceBytes = 8ull << 20;
+
+static int build_graph_parallel(const SegTable& t, cudaGraphExec_t* exec) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaGraphCreate(&graph, 0);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphCreate");
+    auto fail = [&](cudaError_t err, const char* what) {
+        cudaGraphDestroy(graph);
+        return set_cuda_error(err, what);
+    };
+    cudaGraphNode_t node;
+    if (t.kind == kSegAllToAll && t.nranks >= 1) {
+        const int R = t.nranks;
+        const size_t B = (size_t)t.seg_bytes;
+        for (int i = 0; i < R; ++i) {
+            cudaMemcpy3DParms prm = {};
+            prm.srcPtr = make_cudaPitchedPtr(const_cast<uint8_t*>(t.src[i * R]), B, B, (size_t)R);
+            prm.dstPtr = make_cudaPitchedPtr(t.dst[i * R], (size_t)R * B, B, (size_t)R);
+            prm.extent = make_cudaExtent(B, (size_t)R, 1);
+            prm.kind = cudaMemcpyDeviceToDevice;
+            e = cudaGraphAddMemcpyNode(&node, graph, nullptr, 0, &prm);
+            if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode (2-D)");
+        }
+    } else {
+        uint64_t pieces = t.seg_bytes / kPieceBytes;
+        const uint64_t max_pieces = (uint64_t)(64 / (t.nseg > 0 ? t.nseg : 1));
+        if (pieces > max_pieces) pieces = max_pieces;
+        if (pieces < 1) pieces = 1;
+        const uint64_t step = ((t.seg_bytes / pieces) + 15) & ~15ull;
+        for (int i = 0; i < t.nseg; ++i)
+            for (uint64_t off = 0; off < t.seg_bytes; off += step) {
+                const uint64_t n = (t.seg_bytes - off) < step ? (t.seg_bytes - off) : step;
+                e = cudaGraphAddMemcpyNode1D(&node, graph, nullptr, 0, t.dst[i] + off, t.src[i] + off, (size_t)n,
+                                             cudaMemcpyDeviceToDevice);
+                if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode1D");
+            }
+    }
+    e = cudaGraphInstantiate(exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphInstantiate");
+    return 0;
+}
+
+// The STRIDED calls captured from one stream: the copy nodes form a chain in
+// issue order, exactly like the stream-issued variants.
+static int build_graph_captured(const SegTable& t, cudaStream_t capture_stream, cudaGraphExec_t* exec) {
+    cudaError_t e = cudaStreamBeginCapture(capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaStreamBeginCapture");
+    int rc = ce_strided(t, capture_stream);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(capture_stream, &graph);
+    if (rc) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaStreamEndCapture");
+    e = cudaGraphInstantiate(exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphInstantiate");
+    return 0;
+}
+
+static int ce_graph(const SegTable& t, bool parallel, cudaStream_t s, cudaStream_t capture_stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
     GraphEntry* hit = nullptr;
     for (auto& g : g_graphs)
-        if (g.used && g.device == dev && same_table(g.key, t)) hit = &g;
+        if (g.used && g.device == dev && g.parallel == parallel && same_table(g.key, t)) hit = &g;
     if (!hit) {
         GraphEntry* victim = &g_graphs[0];
         for (auto& g : g_graphs) {
@@ -84,20 +159,11 @@ static int ce_graph(const SegTable& t, cudaStream_t s, cudaStream_t capture_stre
         }
         if (victim->used && victim->exec) cudaGraphExecDestroy(victim->exec);
         *victim = GraphEntry();
-        e = cudaStreamBeginCapture(capture_stream, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaStreamBeginCapture");
-        int rc = ce_strided(t, capture_stream);
-        cudaGraph_t graph = nullptr;
-        e = cudaStreamEndCapture(capture_stream, &graph);
-        if (rc) {
-            if (graph) cudaGraphDestroy(graph);
-            return rc;
-        }
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaStreamEndCapture");
-        e = cudaGraphInstantiate(&victim->exec, graph, 0);
-        cudaGraphDestroy(graph);
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphInstantiate");
+        int rc = parallel ? build_graph_parallel(t, &victim->exec)
+                          : build_graph_captured(t, capture_stream, &victim->exec);
+        if (rc) return rc;
         victim->used = true;
+        victim->parallel = parallel;
         victim->device = dev;
         victim->key = t;
         hit = victim;
@@ -111,7 +177,8 @@ static int ce_graph(const SegTable& t, cudaStream_t s, cudaStream_t capture_stre
 int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream) {
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
     if (variant == kCeStrided) return ce_strided(t, s);
-    if (variant == kCeGraph) return ce_graph(t, s, capture_stream);
+    if (variant == kCeGraph) return ce_graph(t, false, s, capture_stream);
+    if (variant == kCeGraphParallel) return ce_graph(t, true, s, capture_stream);
     return ce_per_segment(t, s);
 }
 

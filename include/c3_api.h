@@ -87,11 +87,22 @@ typedef enum { C3_L2_NORMAL = 0, C3_L2_EVICT_FIRST = 1 } c3_l2_policy;
  * the all-to-all).  STRIDED: the all-to-all as R cudaMemcpy2DAsync calls, one
  * per source rank (all-gathers as PER_SEGMENT).  GRAPH: the STRIDED calls
  * captured once into a CUDA graph, cached by buffer addresses and size (up to
- * 16 graphs, released by c3_shutdown), replayed with one launch.  The pages'
- * DMA collectives lose to the compute-unit library below 32 MB on launch and
- * synchronisation cost (Figure 9); STRIDED and GRAPH cut the number of host
- * calls per collective. */
-typedef enum { C3_CE_PER_SEGMENT = 0, C3_CE_STRIDED = 1, C3_CE_GRAPH = 2 } c3_ce_variant;
+ * 16 graphs, released by c3_shutdown), replayed with one launch.
+ * GRAPH_PARALLEL: a cached CUDA graph of independent copy nodes (the 2-D
+ * copies for the all-to-all; 1-D pieces of >= 8 MiB of each segment
+ * otherwise, at most 64 nodes) that the driver spreads over several copy
+ * engines.  Measured on GB300: alone it moves a >= 128 MiB all-gather as fast
+ * as the SM kernel (5.8 TB/s at 256 MiB), but a GEMM running beside it slows
+ * far more than beside the other variants, and later concurrent runs in the
+ * same process do too -- opt-in only.  The pages' DMA collectives lose to the
+ * compute-unit library below 32 MB on launch and synchronisation cost (Figure
+ * 9); STRIDED and GRAPH cut the number of host calls per collective. */
+typedef enum {
+    C3_CE_PER_SEGMENT = 0,
+    C3_CE_STRIDED = 1,
+    C3_CE_GRAPH = 2,
+    C3_CE_GRAPH_PARALLEL = 3
+} c3_ce_variant;
 
 /* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
 typedef enum { C3_CLASS_G_LONG = 0, C3_CLASS_GC_EQUAL = 1, C3_CLASS_C_LONG = 2 } c3_class;

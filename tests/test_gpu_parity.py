@@ -187,7 +187,7 @@ def test_alltoall_streaming_variants_bit_exact(c3, l2):
     assert np.array_equal(out.cpu().numpy(), oracle.alltoall(send, 8))
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
 @pytest.mark.parametrize("coll,unit", [("allgather", 1 << 20), ("allgather", 4096 + 48),
                                        ("alltoall", 128 * 1024), ("alltoall", 1024 + 16)])
 def test_copy_engine_variants_bit_exact(c3, variant, coll, unit):
