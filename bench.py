@@ -76,16 +76,23 @@ def parse_args(argv=None):
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
     ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
     ap.add_argument("--ce-variant", choices=["per_segment", "strided", "graph", "graph_parallel"], default="graph",
-                    help="how the copy-engine modes issue their transfers")
+                    help="how the copy-engine (driver memcpy) modes issue their transfers")
+    ap.add_argument("--coll-src", choices=["device", "host"], default="device",
+                    help="where the collective's sources live: device memory (the emulated ranks inside one HBM) "
+                         "or page-locked host memory (the remote ranks across the CPU-GPU link, reached by "
+                         "host-to-device DMA on the memcpy path and by loads over the link on the SM path); "
+                         "host implies --no-aux and --no-e2e")
     ap.add_argument("--coll-l2", choices=["normal", "evict_first"], default="normal",
                     help="L2 policy of the SM collective's loads and stores")
     ap.add_argument("--heuristics", action="store_true",
                     help="instead of the headline line: calibrate the SM-split slowdown table once, then compare the "
                          "split the pages' heuristic predicts with the swept best over the size sweep")
-    ap.add_argument("--profile-range", choices=["gemm", "baseline", "ce"], default=None,
+    ap.add_argument("--profile-range", choices=["gemm", "baseline", "ce", "sm_only", "ce_only", "ce_parallel_only"],
+                    default=None,
                     help="instead of the headline line: run one phase (the GEMM alone, or the GEMM concurrent with "
-                         "the SM collective / the copy engines) between cudaProfilerStart and cudaProfilerStop, for "
-                         "ncu --replay-mode app-range --profile-from-start off")
+                         "the SM collective / the driver memcpy; or the collective alone on either) between cudaProfilerStart and "
+                         "cudaProfilerStop, for "
+                         "ncu --replay-mode app-range")
     ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
                     help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
     return ap.parse_args(argv)
@@ -104,6 +111,42 @@ def pct_gain(tg, tc, tconc):
     gain = (s_real - 1.0) / (s_ideal - 1.0) if s_ideal > 1.0 else float("nan")
     return {"s_ideal": s_ideal, "s_real": s_real, "pct_ideal_gain": 100.0 * gain,
             "pct_ideal_ratio": 100.0 * s_real / s_ideal}
+
+
+def expected_collective(np, w, payload):
+    """The collective's output bytes from its definition, for post-run
+    validation: rank-order concatenation (all-gather), the block transpose
+    (all-to-all), or every rank holding the rank-order fp32 sum (all-reduce)."""
+    if w.coll == "allgather":
+        return np.concatenate([np.asarray(x).view(np.uint8).reshape(-1) for x in payload])
+    if w.coll == "alltoall":
+        R = w.nranks
+        return np.asarray(payload).reshape(R, R, -1).transpose(1, 0, 2).reshape(-1)
+    acc = np.zeros_like(payload[0], dtype=np.float32)
+    for v in payload:
+        acc = (acc + v).astype(np.float32)
+    return np.tile(acc, len(payload)).view(np.uint8)
+
+
+def gemm_rows_ok(np, A_bits, B_bits, rows, C_rows):
+    """Sampled GEMM rows within |C - exact| <= 1e-4 * sum_k |a b|: the bf16
+    operands widened exactly, products and sums in fp64 (numpy)."""
+    def widen(u16):
+        return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    A, B = widen(A_bits[rows]), widen(B_bits)
+    ref = A @ B.T
+    bound = 1e-4 * (np.abs(A) @ np.abs(B).T)
+    C = np.asarray(C_rows, dtype=np.float64)
+    return bool(np.isfinite(C).all() and (np.abs(C - ref) <= bound).all())
+
+
+def c3_class(tg, tc):
+    """Taxonomy class of a pair (Section III: 115% / 15% thresholds)."""
+    if tg >= 1.15 * tc:
+        return "G-long"
+    if tc >= 1.15 * tg:
+        return "C-long"
+    return "GC-equal"
 
 
 def strict_comm_time(per_mode, modes):
@@ -417,9 +460,8 @@ def run_sweep(args, c3, torch, np, I, dev, info):
             dsh = [torch.from_numpy(x).to(dev) for x in payload]
             dsend, cid, ref = None, c3.C3_COLL_ALLGATHER, np.concatenate(payload)
         else:
-            import oracle
             dsh, dsend, cid = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
-            ref = oracle.alltoall(payload, w.nranks)
+            ref = expected_collective(np, w, payload)
         out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
         prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, cid, out, w.unit_bytes, w.nranks, shards=dsh, send=dsend,
                           flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
@@ -442,7 +484,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
             res[name] = {"t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc, "t_comm_strict_us": 1e6 * tc_strict,
                          "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"],
                          "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
-                         "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "class": recs[0]["class"]}
+                         "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "class": c3_class(tg, tc_strict)}
         best = max(res, key=lambda k: res[k]["pct_ideal_gain"] if res[k]["s_ideal"] > 1.0 else -1e9)
         print(json.dumps({"sweep": args.sweep, "workload": w.name, "coll_bytes": w.coll_bytes, "steps": args.steps,
                           "collective_bit_exact": exact, "best_mode": best, "modes": res}), flush=True)
@@ -576,12 +618,25 @@ def main(argv=None):
     dA = torch.from_numpy(A_h.view(np.int16)).to(dev)
     dB = torch.from_numpy(B_h.view(np.int16)).to(dev)
     dC = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    host_src = args.coll_src == "host"
+    if host_src:
+        if w.coll == "allreduce":
+            raise SystemExit("--coll-src host: the all-reduce's inputs feed an SM reduction and stay in HBM")
+        args.no_aux = args.no_e2e = True
+
+    def place(a):
+        if not host_src:
+            return torch.from_numpy(a).to(dev)
+        t = torch.empty(a.shape, dtype=torch.from_numpy(a[:0]).dtype, pin_memory=True)
+        t.copy_(torch.from_numpy(a))
+        return t
+
     if w.coll in ("allgather", "allreduce"):
-        dshards = [torch.from_numpy(s).to(dev) for s in payload]
+        dshards = [place(s) for s in payload]
         dsend = None
         coll_id = c3.C3_COLL_ALLGATHER if w.coll == "allgather" else c3.C3_COLL_ALLREDUCE
     else:
-        dshards, dsend, coll_id = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
+        dshards, dsend, coll_id = None, place(payload), c3.C3_COLL_ALLTOALL
     out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -596,10 +651,21 @@ def main(argv=None):
             c3.c3_run(prob, c3.C3_MODE_CONCURRENT_CE, 0, 0)
         c3.c3_l2_flush(flush, flush.numel(), stream)
         torch.cuda.synchronize(dev)
+        only = {"sm_only": (c3.C3_MODE_SERIAL_SM, c3.C3_CE_GRAPH),
+                "ce_only": (c3.C3_MODE_SERIAL_CE, ce_variant_arg(args, c3)),
+                "ce_parallel_only": (c3.C3_MODE_SERIAL_CE, c3.C3_CE_GRAPH_PARALLEL)}.get(args.profile_range)
+        if only:
+            # the collective alone (an empty GEMM), so the range holds nothing else
+            cprob = c3.Problem(None, None, None, 0, 0, 0, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
+                               send=dsend, stream=stream, ce_variant=only[1])
+            c3.c3_run(cprob, only[0], 0, 0)   # builds and caches the graph outside the range
+            torch.cuda.synchronize(dev)
         torch.cuda.profiler.start()
         if args.profile_range == "gemm":
             c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
             torch.cuda.synchronize(dev)
+        elif only:
+            c3.c3_run(cprob, only[0], 0, 0)
         else:
             c3.c3_run(prob, c3.C3_MODE_CONCURRENT_SM if args.profile_range == "baseline" else c3.C3_MODE_CONCURRENT_CE,
                       0, 0)
@@ -632,18 +698,10 @@ def main(argv=None):
     ms_per_step = reduce_max(pg, ms_per_step, dev)
 
     # ---- post-run validation (every mode ran on these buffers; check the last outputs)
-    import oracle
-    if w.coll == "allreduce":
-        coll_ok = bool(np.array_equal(out.cpu().numpy().view(np.uint32),
-                                      oracle.allreduce(payload)[0].reshape(-1).view(np.uint32)))
-    elif w.coll == "allgather":
-        coll_ok = bool(np.array_equal(out.cpu().numpy(), np.concatenate(payload)))
-    else:
-        coll_ok = bool(np.array_equal(out.cpu().numpy(), oracle.alltoall(payload, w.nranks)))
+    coll_ok = bool(np.array_equal(out.cpu().numpy().view(np.uint8), expected_collective(np, w, payload)))
     rows = np.array([0, 1, w.M // 2, w.M - 1])
-    Cref, Sref = oracle.gemm(A_h[rows], B_h)
-    Cg = dC[torch.from_numpy(rows).to(dev)].cpu().numpy().astype(np.float64)
-    gemm_ok = bool((np.abs(Cg - Cref) <= 1e-4 * Sref).all())
+    Cg = dC[torch.from_numpy(rows).to(dev)].cpu().numpy()
+    gemm_ok = gemm_rows_ok(np, A_h, B_h, rows, Cg)
 
     # ---- statistics per mode (medians over the timed steps)
     stats = {}
@@ -657,7 +715,7 @@ def main(argv=None):
         m_own = pct_gain(tg, tc, tconc)
         tgd = statistics.median(r["t_gemm_dev"] for r in recs)
         # the SM collective's own kernel window when it is all on SMs; fork-to-done
-        # events when copy engines carry all or part of it
+        # events when the memcpy path carries all or part of it
         tcd = [r["t_comm_dev"] if (r["comm_ctas"] and r["mode"] in (0, 1)) else r["t_comm_ev"] for r in recs]
         stats[name] = {
             "t_gemm_iso_us": 1e6 * tg, "t_comm_iso_us": 1e6 * tc, "t_comm_iso_strict_us": 1e6 * tc_strict,
@@ -667,9 +725,10 @@ def main(argv=None):
             "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
             "pct_ideal_gain_own_engine_per_step": spread([100.0 * r["pct_ideal_gain"] for r in recs]),
-            "class": recs[0]["class"],
+            "class": c3_class(tg, tc_strict), "class_own_engine": c3_class(tg, tc),
             "gemm_tflops_overlap": w.gemm_flops / tgd / 1e12 if tgd > 0 else None,
-            "copy_gbs_overlap": w.coll_traffic_bytes / statistics.median(tcd) / 1e9 if statistics.median(tcd) > 0 else None,
+            "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / statistics.median(tcd) / 1e9
+                                 if statistics.median(tcd) > 0 else None),
             "gemm_slowdown": tgd / tg if tg > 0 else None,
             "gemm_ctas": recs[0]["gemm_ctas"], "comm_ctas": recs[0]["comm_ctas"],
             "smid_overlap_max": max(r["smid_overlap"] for r in recs),
@@ -696,7 +755,13 @@ def main(argv=None):
     roof["peak_source"] = f"{peaks['source']} (burst)"
     tc_sm = statistics.median(r["t_comm_iso"] for r in per_mode["baseline"]) if "baseline" in per_mode else None
     copy_roof = None
-    if tc_sm:
+    if tc_sm and host_src:
+        # the sources cross the CPU-GPU link: the link, not HBM, bounds the copy,
+        # and no measured peak of it is at hand
+        gbs = w.coll_bytes / tc_sm / 1e9
+        copy_roof = {"bound": "cpu-gpu link", "achieved": gbs, "peak": None, "unit": "GB/s (bytes delivered)",
+                     "frac": None, "kernel": "copy_vec_kernel (default budget), sources in page-locked host memory"}
+    elif tc_sm:
         gbs = w.coll_traffic_bytes / tc_sm / 1e9
         copy_roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"],
@@ -713,6 +778,8 @@ def main(argv=None):
                          f"half read back so L2 holds clean lines)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "coll_l2": args.coll_l2, "ce_variant": args.ce_variant,
+                   "coll_src": ("page-locked host memory (remote ranks across the CPU-GPU link)" if host_src
+                                else "device memory (8 emulated ranks in one HBM)"),
                    "modes": [m[0] for m in modes]},
         "best_mode": best,
         "gemm_tflops_overlap": stats[best]["gemm_tflops_overlap"],
@@ -763,7 +830,7 @@ def _event_time(torch, stream, fn, reps, warm, flush=None):
 def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
     """Isolated kernel rates beside the C3 line: the GEMM on the compute-bound
     shapes of the other workloads (TFLOP/s vs the dense bf16 peak), and the
-    collective's GB/s per SM budget for both SM kernels and the copy engines
+    collective's GB/s per SM budget for both SM kernels and the driver memcpy
     (the pages' Figure 5b/c question: how many compute units a collective
     needs)."""
     res = {"gemm": {}, "copy_gbs_by_sms": {}}

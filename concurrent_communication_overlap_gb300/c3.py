@@ -1,9 +1,10 @@
 """Python binding of libc3.so (include/c3_api.h): argument marshalling only.
 
 Every function has the C entry point's name and meaning; tensors are passed
-as device pointers (``tensor.data_ptr()``), streams as ``cudaStream_t``
-handles (``torch.cuda.Stream.cuda_stream``).  All work runs in the library's
-CUDA kernels or copy-engine transfers; nothing here computes.  Importing this
+as pointers (``tensor.data_ptr()``: device memory, or page-locked host memory
+for a collective's sources), streams as ``cudaStream_t`` handles
+(``torch.cuda.Stream.cuda_stream``).  All work runs in the library's CUDA
+kernels or in driver memcpy transfers; nothing here computes.  Importing this
 module raises ImportError when libc3.so has not been built: there is no
 fallback path.
 """
@@ -120,7 +121,7 @@ def lib():
 
 
 def _ptr(x):
-    """Device pointer of a tensor (``data_ptr``), an int, or None."""
+    """Address of a tensor (``data_ptr``), an int, or None."""
     if x is None:
         return None
     if isinstance(x, int):

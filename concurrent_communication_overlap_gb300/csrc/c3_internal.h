@@ -69,7 +69,7 @@ struct SegTable {
     int kind;       // kSegAllGather or kSegAllToAll
     uint64_t seg_bytes;
     int nranks;
-    int pad;
+    int host_src;   // 1: at least one source is page-locked host memory (src[] holds its device address)
 };
 
 enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2, kCeGraphParallel = 3 };

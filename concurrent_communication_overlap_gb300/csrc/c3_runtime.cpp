@@ -234,6 +234,72 @@ static int build_allreduce(const void* const* inputs, void* out, size_t count, i
     return C3_OK;
 }
 
+// Where one buffer lives.  Device memory of the current device (or managed
+// memory) is used as given.  Page-locked host memory (cudaHostAlloc, or
+// cudaHostRegister) is accepted as a collective's SOURCE only: the segment
+// table then holds its device address, the copy engines reach it with
+// host-to-device DMA and the SM copy kernel with plain loads over the CPU-GPU
+// link.  Pageable memory and another device's memory are argument errors.
+static int locate(const void* p, int dev, bool allow_host, bool* host, const void** dptr) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaPointerGetAttributes");
+    *host = false;
+    *dptr = p;
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        if (a.type == cudaMemoryTypeDevice && a.device != dev)
+            return set_error(C3_EINVAL, "a buffer belongs to another device");
+        return C3_OK;
+    }
+    if (a.type == cudaMemoryTypeHost) {
+        if (!allow_host) return set_error(C3_EINVAL, "only a collective's sources may be host memory");
+        if (!a.devicePointer) return set_error(C3_EINVAL, "page-locked host buffer has no device mapping");
+        // the device address keeps the host address's offset within the allocation
+        *host = true;
+        *dptr = a.devicePointer;
+        return C3_OK;
+    }
+    return set_error(C3_EINVAL, "a buffer is pageable host memory: use device or page-locked host memory");
+}
+
+// Resolves every buffer of a built plan against the current device: the
+// destinations must be device memory; all-gather and all-to-all sources may
+// be page-locked host memory (the all-reduce's inputs feed an SM reduction
+// and must be device memory).
+static int locate_plan(const DeviceState& ds, CollPlan* cp) {
+    SegTable& t = cp->seg;
+    t.host_src = 0;
+    bool host = false;
+    const void* d = nullptr;
+    int rc;
+    if (cp->has_rs) {
+        for (int q = 0; q < cp->rs.nranks; ++q)
+            if ((rc = locate(cp->rs.in[q], ds.device, false, &host, &d))) return rc;
+        return locate(cp->rs.out, ds.device, false, &host, &d);
+    }
+    if (t.nseg == 0 || t.seg_bytes == 0) return C3_OK;
+    if (t.kind == kSegAllToAll) {
+        // one send buffer and one receive buffer; block (0,0) sits at both bases
+        if ((rc = locate(t.dst[0], ds.device, false, &host, &d))) return rc;
+        if ((rc = locate(t.src[0], ds.device, true, &host, &d))) return rc;
+        if (host) {
+            const intptr_t shift = (const uint8_t*)d - t.src[0];
+            for (int i = 0; i < t.nseg; ++i) t.src[i] += shift;
+            t.host_src = 1;
+        }
+        return C3_OK;
+    }
+    if ((rc = locate(t.dst[0], ds.device, false, &host, &d))) return rc;
+    for (int i = 0; i < t.nseg; ++i) {
+        if ((rc = locate(t.src[i], ds.device, true, &host, &d))) return rc;
+        if (host) {
+            t.src[i] = static_cast<const uint8_t*>(d);
+            t.host_src = 1;
+        }
+    }
+    return C3_OK;
+}
+
 // One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
 // the CTAs keep their SMs to themselves (partitioning).
 static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_kernel, int l2_stream, int ce_variant,
@@ -258,9 +324,11 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
     if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
     int k = budget > 0 ? budget : default_comm_sms(ds);
     if (k > ds.sm_count) k = ds.sm_count;
+    if (t.host_src && sm_kernel == C3_SMK_BULK)
+        return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only; host sources take the vector kernel");
     int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
                   : sm_kernel == C3_SMK_BULK ? kSmkBulk
-                  : (exclusive ? kSmkBulk : kSmkVec);
+                  : (exclusive && !t.host_src ? kSmkBulk : kSmkVec);
     int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
     return copy_sm_launch(t, k, flavour, reserve, l2_stream, s, ds.status, ctas);
 }
@@ -547,6 +615,7 @@ int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int n
     if (shard_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
+    if ((rc = locate_plan(*ds, &t))) return rc;
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
@@ -560,6 +629,7 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     if (block_bytes == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
+    if ((rc = locate_plan(*ds, &t))) return rc;
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
@@ -592,6 +662,7 @@ int c3_allreduce(const float* const* inputs, float* out, size_t count, int nrank
     if (count == 0) return C3_OK;
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
+    if ((rc = locate_plan(*ds, &t))) return rc;
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s),
                        nullptr);
 }
@@ -613,6 +684,9 @@ int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing*
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
     if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
+    if ((rc = locate_plan(*ds, &t))) return rc;
+    if (t.seg.host_src && p->sm_kernel == C3_SMK_BULK)
+        return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only");
     out->mode = mode;
     out->sm_split = sm_split;
     out->priority = priority;
@@ -632,6 +706,9 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
     if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
+    if ((rc = locate_plan(*ds, &t))) return rc;
+    if (t.seg.host_src && p->sm_kernel == C3_SMK_BULK)
+        return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only");
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
     for (int it = 0; it < warmup + reps; ++it) {

@@ -1,16 +1,22 @@
-// ce_offload.cpp -- the collective as copy-engine transfers (the DMA offload).
+// ce_offload.cpp -- the collective as driver memcpy transfers (the DMA-offload mode).
 //
 // ConCCL breaks each collective into individual transfers and hands them to
 // the GPU's DMA engines from the CPU, so that no compute unit and no L1/L2
 // capacity is spent on the data movement ("Optimizing ML Concurrent
 // Computation and Communication with GPU DMA Engines", pith.science paper
 // page, "What carries the argument"; Sections VI-A/VI-B).  CUDA exposes no
-// per-engine queue; the portable equivalent is device-to-device
-// cudaMemcpyAsync on a dedicated stream, which the driver gives to a copy
-// engine.  Whether any SM kernel ran for these transfers is checked by
-// profiling (kernel launch list) rather than assumed.
+// per-engine queue.  This file issues the transfers through cudaMemcpyAsync
+// and its 2-D and graph forms on a dedicated stream, and lets the driver pick
+// the engine (cudaMemcpyDefault, so a source may also be page-locked host
+// memory).
 //
-// Three ways to issue them (the pages' DMA path is 4x slower than the
+// Which engine the driver picks is measured, not assumed.  On GB300 with
+// driver 580 a copy between two device buffers of the same GPU runs as
+// driver-internal SM work: its profiled range executes SM instructions and
+// reads the collective's bytes through L1/TEX, in every form below.  A copy
+// whose source is page-locked host memory is host-to-device DMA.
+//
+// The ways to issue the transfers (the pages' DMA path is 4x slower than the
 // CU-based library below 32 MB because of launch and synchronisation cost,
 // Figure 9; the variants below attack that cost):
 //   PER_SEGMENT  one cudaMemcpyAsync per segment (8 for an all-gather, R^2 for
@@ -20,11 +26,11 @@
 //   GRAPH        the STRIDED calls captured once into a CUDA graph (cached by
 //                buffer addresses and size) and replayed with one launch.
 //   GRAPH_PARALLEL  a CUDA graph of independent copy nodes (strided 2-D nodes
-//                for the all-to-all, 1-D pieces otherwise): with no edges the
-//                driver spreads them over several copy engines.  Measured on
-//                GB300: as fast as the SM kernel alone for all-gathers of
-//                >= 128 MiB, but a concurrent GEMM runs much slower beside it,
-//                and so do later concurrent runs in the same process.  Opt-in.
+//                for the all-to-all, 1-D pieces otherwise), which the driver
+//                may run at the same time.  Measured on GB300: as fast as the
+//                SM kernel alone for all-gathers of >= 128 MiB, but a
+//                concurrent GEMM runs much slower beside it, and so do later
+//                concurrent runs in the same process.  Opt-in.
 #include "c3_internal.h"
 
 #include <cstring>
@@ -33,8 +39,8 @@ namespace c3 {
 
 static int ce_per_segment(const SegTable& t, cudaStream_t s) {
     for (int i = 0; i < t.nseg; ++i) {
-        cudaError_t e = cudaMemcpyAsync(t.dst[i], t.src[i], (size_t)t.seg_bytes, cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpyAsync (copy engine)");
+        cudaError_t e = cudaMemcpyAsync(t.dst[i], t.src[i], (size_t)t.seg_bytes, cudaMemcpyDefault, s);
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpyAsync (collective segment)");
     }
     return 0;
 }
@@ -47,8 +53,8 @@ static int ce_strided(const SegTable& t, cudaStream_t s) {
         // source rank i: blocks j = 0..R-1 contiguous at src[i*R]; block j goes to
         // dst[i*R + j] = out + (j*R + i)*B, i.e. R*B apart starting at dst[i*R].
         cudaError_t e = cudaMemcpy2DAsync(t.dst[i * R], (size_t)R * B, t.src[i * R], B, B, (size_t)R,
-                                          cudaMemcpyDeviceToDevice, s);
-        if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpy2DAsync (copy engine)");
+                                          cudaMemcpyDefault, s);
+        if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpy2DAsync (collective rank)");
     }
     return 0;
 }
@@ -74,11 +80,11 @@ static bool same_table(const SegTable& a, const SegTable& b) {
 }
 
 // Builds a graph directly, with no edges between the copy nodes, so that the
-// driver may run them on several copy engines at once (a stream-captured graph
-// would chain them in issue order).  The all-to-all uses one strided 2-D node
+// driver may run them at the same time (a stream-captured graph would chain
+// them in issue order).  The all-to-all uses one strided 2-D node
 // per source rank; other collectives one 1-D node per segment, each segment
 // cut into pieces of at least kPieceBytes when there is room (at most 64
-// nodes), to spread large transfers over more engines.
+// nodes), so that large transfers can proceed in parallel.
 constexpr uint64_t kPieceBytes = 8ull << 20;
 
 static int build_graph_parallel(const SegTable& t, cudaGraphExec_t* exec) {
@@ -98,7 +104,7 @@ static int build_graph_parallel(const SegTable& t, cudaGraphExec_t* exec) {
             prm.srcPtr = make_cudaPitchedPtr(const_cast<uint8_t*>(t.src[i * R]), B, B, (size_t)R);
             prm.dstPtr = make_cudaPitchedPtr(t.dst[i * R], (size_t)R * B, B, (size_t)R);
             prm.extent = make_cudaExtent(B, (size_t)R, 1);
-            prm.kind = cudaMemcpyDeviceToDevice;
+            prm.kind = cudaMemcpyDefault;
             e = cudaGraphAddMemcpyNode(&node, graph, nullptr, 0, &prm);
             if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode (2-D)");
         }
@@ -112,7 +118,7 @@ static int build_graph_parallel(const SegTable& t, cudaGraphExec_t* exec) {
             for (uint64_t off = 0; off < t.seg_bytes; off += step) {
                 const uint64_t n = (t.seg_bytes - off) < step ? (t.seg_bytes - off) : step;
                 e = cudaGraphAddMemcpyNode1D(&node, graph, nullptr, 0, t.dst[i] + off, t.src[i] + off, (size_t)n,
-                                             cudaMemcpyDeviceToDevice);
+                                             cudaMemcpyDefault);
                 if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode1D");
             }
     }

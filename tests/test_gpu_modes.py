@@ -84,7 +84,7 @@ def test_mode_runs_and_outputs_are_exact(c3, setup, name, mode, split, prio):
     t = c3.c3_run(setup.p, mode, split, prio)
     assert t["status"] == 0 and t["t_conc"] > 0
     assert t["gemm_ctas"] >= 1
-    if mode in (2, 3):  # copy engines: no collective kernel ran
+    if mode in (2, 3):  # memcpy path: no collective kernel of this library ran
         assert t["comm_ctas"] == 0 and t["comm_sms"] == 0
     else:
         assert t["comm_ctas"] >= 1 and t["comm_sms"] >= 1
