@@ -95,6 +95,9 @@ def parse_args(argv=None):
                          "ncu --replay-mode app-range")
     ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
                     help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
+    ap.add_argument("--sweep-max-mib", type=int, default=1024,
+                    help="largest collective total of the sweep, MiB (power of two; above 1024 extends the pages' "
+                         "range so that the device-resident sweep also reaches GC-equal and C-long pairs)")
     return ap.parse_args(argv)
 
 
@@ -111,6 +114,16 @@ def pct_gain(tg, tc, tconc):
     gain = (s_real - 1.0) / (s_ideal - 1.0) if s_ideal > 1.0 else float("nan")
     return {"s_ideal": s_ideal, "s_real": s_real, "pct_ideal_gain": 100.0 * gain,
             "pct_ideal_ratio": 100.0 * s_real / s_ideal}
+
+
+def place_source(torch, a, dev, host):
+    """A collective source buffer: in HBM, or in page-locked host memory when
+    `host` (the remote ranks across the CPU-GPU link)."""
+    if not host:
+        return torch.from_numpy(a).to(dev)
+    t = torch.empty(a.shape, dtype=torch.from_numpy(a[:0]).dtype, pin_memory=True)
+    t.copy_(torch.from_numpy(a))
+    return t
 
 
 def expected_collective(np, w, payload):
@@ -446,7 +459,14 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     prioritised, partitioned_32, ce), one JSON line per size."""
     names = args.modes.split(",") if args.modes else ["baseline", "prioritised", "partitioned_32", "reclaim_16", "ce"]
     modes = [m for m in MODES if m[0] in names]
-    ws = I.sweep_workloads(args.sweep)
+    if args.sweep_max_mib < 1 or args.sweep_max_mib & (args.sweep_max_mib - 1):
+        raise SystemExit("--sweep-max-mib must be a power of two")
+    ws = I.sweep_workloads(args.sweep, hi_bytes=args.sweep_max_mib << 20)
+    host_src = args.coll_src == "host"
+
+    def place(a):
+        return place_source(torch, a, dev, host_src)
+
     w0 = ws[0]
     A_h, B_h = I.gemm_operands(w0)
     dA = torch.from_numpy(A_h.view(np.int16)).to(dev)
@@ -457,10 +477,10 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     for w in ws:
         payload = I.coll_payload(w)
         if w.coll == "allgather":
-            dsh = [torch.from_numpy(x).to(dev) for x in payload]
+            dsh = [place(x) for x in payload]
             dsend, cid, ref = None, c3.C3_COLL_ALLGATHER, np.concatenate(payload)
         else:
-            dsh, dsend, cid = None, torch.from_numpy(payload).to(dev), c3.C3_COLL_ALLTOALL
+            dsh, dsend, cid = None, place(payload), c3.C3_COLL_ALLTOALL
             ref = expected_collective(np, w, payload)
         out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
         prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, cid, out, w.unit_bytes, w.nranks, shards=dsh, send=dsend,
@@ -487,6 +507,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
                          "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "class": c3_class(tg, tc_strict)}
         best = max(res, key=lambda k: res[k]["pct_ideal_gain"] if res[k]["s_ideal"] > 1.0 else -1e9)
         print(json.dumps({"sweep": args.sweep, "workload": w.name, "coll_bytes": w.coll_bytes, "steps": args.steps,
+                          "coll_src": args.coll_src,
                           "collective_bit_exact": exact, "best_mode": best, "modes": res}), flush=True)
         del out, dsh, dsend, prob
     return 0
@@ -625,11 +646,7 @@ def main(argv=None):
         args.no_aux = args.no_e2e = True
 
     def place(a):
-        if not host_src:
-            return torch.from_numpy(a).to(dev)
-        t = torch.empty(a.shape, dtype=torch.from_numpy(a[:0]).dtype, pin_memory=True)
-        t.copy_(torch.from_numpy(a))
-        return t
+        return place_source(torch, a, dev, host_src)
 
     if w.coll in ("allgather", "allreduce"):
         dshards = [place(s) for s in payload]
@@ -725,6 +742,7 @@ def main(argv=None):
             "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
             "pct_ideal_gain_own_engine_per_step": spread([100.0 * r["pct_ideal_gain"] for r in recs]),
+            "spread_us": {k: spread([1e6 * r[k] for r in recs]) for k in ("t_gemm_iso", "t_comm_iso", "t_conc")},
             "class": c3_class(tg, tc_strict), "class_own_engine": c3_class(tg, tc),
             "gemm_tflops_overlap": w.gemm_flops / tgd / 1e12 if tgd > 0 else None,
             "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / statistics.median(tcd) / 1e9
