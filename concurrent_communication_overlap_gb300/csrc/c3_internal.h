@@ -126,7 +126,8 @@ struct GemmLaunch {
     int64_t M = 0, N = 0, K = 0;
     int ci = 0, grid = 0, num_kb = 0;
     int64_t num_m = 0, num_n = 0;
-    CUtensorMap ma, mb;
+    int has_mc = 0;  // mc (the fp32 output as a TMA store target) is valid: N % 4 == 0
+    CUtensorMap ma, mb, mc;
 };
 int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
                  GemmLaunch* g);

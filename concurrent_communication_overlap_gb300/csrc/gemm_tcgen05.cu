@@ -14,10 +14,14 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): 4 x tcgen05.mma
 //               (M=128, N=BN, K=16) per stage into one of two TMEM
 //               accumulators, tcgen05.commit frees the stage / publishes the tile;
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, fp32 stores to C
-//               with edge masking, then release the accumulator.
-// The two accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.  Tiles are claimed one by one from an atomic counter (a
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, then out to C.
+//               Staged: each 32 x 32 fp32 block goes through shared memory in
+//               the 128-byte swizzle and leaves by TMA store, whole cache lines
+//               at a time, and the accumulator is released as soon as it has
+//               been read out.  Direct (no staging space for this tile, or
+//               N % 4 != 0): per-thread row stores with edge masking.
+// Two accumulator sets, where TMEM holds them, let the epilogue of tile i
+// overlap the main loop of tile i+1.  Tiles are claimed one by one from an atomic counter (a
 // scheduler slot in the status block), in a grouped order: GROUP_M row blocks
 // advance together so that the tiles in flight share A row blocks and B
 // column blocks in L2.  A CTA slowed by a neighbour, or started late because
@@ -53,8 +57,16 @@ struct GemmCfg {
     static constexpr uint32_t kUsedCols = kAccCols * kAccBufs;
     static constexpr uint32_t kTmemCols = kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128
                                           : kUsedCols <= 256 ? 256 : 512;
-    // ring, then barriers / TMEM slot / abort flag (512 B), plus 1 KiB for alignment
-    static constexpr int kSmem = kStages * kStageBytes + 1024 + 512;
+    // Epilogue staging: two 4 KiB blocks (32 rows x 128 B) per epilogue warp.
+    // Its own region when the ring leaves room for it; otherwise the CTA's
+    // last tile borrows the (then idle) first ring stage, and earlier tiles
+    // store directly.
+    static constexpr int kStagingBytes = 4 * 2 * 4096;
+    static constexpr bool kOwnStaging =
+        kSmemLimit - 1024 - 512 - kStages * (int)kStageBytes >= kStagingBytes;
+    static_assert(kOwnStaging || (int)kStageBytes >= kStagingBytes, "no room to stage the epilogue");
+    // ring, [staging], then barriers / TMEM slot / abort flag (512 B), plus 1 KiB for alignment
+    static constexpr int kSmem = kStages * kStageBytes + (kOwnStaging ? kStagingBytes : 0) + 1024 + 512;
     static_assert(kStages >= 2, "tile too large for the shared-memory ring");
     static_assert(kUsedCols <= 512, "accumulators exceed TMEM");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128 is 16..256 step 16");
@@ -92,8 +104,8 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
 template <int BN, int MSUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     float* __restrict__ C, int M, int N, int num_m, int num_n, int num_kb,
-                     unsigned int* sched, DevStatus* st) {
+                     const __grid_constant__ CUtensorMap tmC, int has_mc, float* __restrict__ C, int M, int N,
+                     int num_m, int num_n, int num_kb, unsigned int* sched, DevStatus* st) {
     using Cfg = GemmCfg<BN, MSUB>;
     constexpr int S = Cfg::kStages;
     constexpr int NB = Cfg::kAccBufs;
@@ -102,8 +114,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    // ring: stage i = [A sub-tile 0 .. MSUB-1][B], then barriers
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * Cfg::kStageBytes);
+    // ring: stage i = [A sub-tile 0 .. MSUB-1][B], then the staging region (if own), then barriers
+    const uint32_t own_staging = base + S * Cfg::kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * Cfg::kStageBytes +
+                                                 (Cfg::kOwnStaging ? Cfg::kStagingBytes : 0));
     // bars[0..S) full, [S..2S) empty, [2S..2S+NB) tmem_full, [2S+NB..2S+2NB) tmem_empty, [2S+2NB] drain,
     // then the tile ring's full and empty barriers
     constexpr int kTR = 4;  // tile-id ring between the producer and the MMA / epilogue roles
@@ -139,6 +153,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_barrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (has_mc) prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), Cfg::kTmemCols);
@@ -285,6 +300,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_REMPTY + slot));
             if (t >= total_tiles) break;
+            // Where this tile's output is staged: the own region, or the first
+            // ring stage when this is the CTA's last tile (the producer then
+            // loads nothing more, and every stage has been consumed once the
+            // accumulator is ready).  The next tile-ring entry is already
+            // published by then: the producer writes it as soon as it has
+            // issued this tile's last load.
+            bool staged = false;
+            uint32_t stg = own_staging;
+            if (has_mc) {
+                if (Cfg::kOwnStaging) {
+                    staged = true;
+                } else {
+                    const int nslot = (local + 1) & (kTR - 1);
+                    const bool seen =
+                        mbar_wait(bar(BAR_RFULL + nslot), (uint32_t)((local + 1) / kTR) & 1u, abort_flag);
+                    if (!__all_sync(0xffffffffu, seen)) {
+                        report_error(st, -4, kSiteGemmEpilogue);
+                        break;
+                    }
+                    staged = tile_ring[nslot] >= total_tiles;
+                    stg = base;
+                }
+            }
             const int buf = local % NB;
             const uint32_t use = (uint32_t)(local / NB);
             // tcgen05.ld is warp-collective: the whole warp leaves together if
@@ -297,36 +335,89 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             int mb, nb;
             tile_coords(t, num_m, num_n, mb, nb);
+            if (staged) {
+                // Two 4 KiB blocks per warp, alternating; a block is rewritten
+                // only after the TMA store issued from it two blocks ago has
+                // read it.  Row `lane` of a block holds 32 fp32 in eight 16-byte
+                // chunks, chunk j at position j ^ (lane & 7): the 128-byte
+                // swizzle the store's tensor map undoes, and no bank conflicts
+                // beyond the four wavefronts 512 bytes need.
+                const uint32_t wstg = stg + (uint32_t)q * 8192u;
+                int issued = 0;
 #pragma unroll 1
-            for (int sub = 0; sub < MSUB; ++sub) {
-                const int row = mb * kRowsCta + sub * kBM + q * 32 + lane;
-                float* crow = C + (size_t)row * (size_t)N;
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)(buf * Cfg::kAccCols + sub * BN);
+                for (int sub = 0; sub < MSUB; ++sub) {
+                    const int row0 = mb * kRowsCta + sub * kBM + q * 32;
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)(buf * Cfg::kAccCols + sub * BN);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(taddr + (uint32_t)(c * 32), r);
-                    tmem_ld_wait();
-                    const int col0 = nb * BN + c * 32;
-                    if (row < M) {
-                        if (vec_ok && col0 + 32 <= N) {
-                            float4* dst = reinterpret_cast<float4*>(crow + col0);
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                        tmem_ld_wait();
+                        if (sub == MSUB - 1 && c == BN / 32 - 1) {
+                            // the accumulator set has been read out: the MMA may reuse it
+                            tc_fence_before();
+                            mbar_arrive(bar(BAR_TEMPTY + buf));
+                        }
+                        const int col0 = nb * BN + c * 32;
+                        if (row0 >= M || col0 >= N) continue;  // wholly outside C (uniform per warp)
+                        const uint32_t blk = wstg + (uint32_t)(issued & 1) * 4096u;
+                        if (issued >= 2) {
+                            if (lane == 0) bulk_wait_read<1>();
+                            __syncwarp();
+                        }
+                        const uint32_t rowp = blk + (uint32_t)lane * 128u;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                        } else {
+                        for (int j = 0; j < 8; ++j)
+                            st_shared_v4(rowp + ((uint32_t)(j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1],
+                                         r[4 * j + 2], r[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, blk, col0, row0);  // clipped to M x N by the tensor map
+                            bulk_commit();
+                        }
+                        ++issued;
+                    }
+                }
+                if (lane == 0) bulk_wait_read<0>();  // staging free for the next tile
+                __syncwarp();
+            } else {
+#pragma unroll 1
+                for (int sub = 0; sub < MSUB; ++sub) {
+                    const int row = mb * kRowsCta + sub * kBM + q * 32 + lane;
+                    float* crow = C + (size_t)row * (size_t)N;
+                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                           (uint32_t)(buf * Cfg::kAccCols + sub * BN);
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(taddr + (uint32_t)(c * 32), r);
+                        tmem_ld_wait();
+                        const int col0 = nb * BN + c * 32;
+                        if (row < M) {
+                            if (vec_ok && col0 + 32 <= N) {
+                                float4* dst = reinterpret_cast<float4*>(crow + col0);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+                                for (int j = 0; j < 8; ++j)
+                                    dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                         __uint_as_float(r[4 * j + 2]),
+                                                         __uint_as_float(r[4 * j + 3]));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+                            }
                         }
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(bar(BAR_TEMPTY + buf));
             }
-            tc_fence_before();
-            mbar_arrive(bar(BAR_TEMPTY + buf));
         }
+        // every TMA store this warp issued has completed before the CTA ends
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -373,6 +464,25 @@ static int make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(-3, "cuTensorMapEncodeTiled failed");
     return 0;
+}
+
+// The fp32 output C [M][N] as a TMA store target: box 32 x 32, the 128-byte
+// swizzle the epilogue writes its staging blocks in.  Needs a row pitch that
+// is a multiple of 16 bytes (N % 4 == 0); returns 1 when the map was made, 0
+// when the epilogue must store directly.
+static int make_out_map(CUtensorMap* map, float* C, int64_t M, int64_t N) {
+    if (N % 4 != 0) return 0;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(-3, "cuTensorMapEncodeTiled entry point unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)N * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(-3, "cuTensorMapEncodeTiled (output) failed");
+    return 1;
 }
 
 // The tile configurations this build carries (BN x MSUB), in the order the
@@ -437,12 +547,13 @@ static int choose_cfg(int64_t M, int64_t N, int64_t K, int cap) {
     return best;
 }
 
-static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, float* C, int64_t M, int64_t N,
-                      int64_t num_m, int64_t num_n, int num_kb, unsigned int* sched, DevStatus* st, cudaStream_t s) {
+static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                      int has_mc, float* C, int64_t M, int64_t N, int64_t num_m, int64_t num_n, int num_kb,
+                      unsigned int* sched, DevStatus* st, cudaStream_t s) {
     const TileCfg& c = kCfgs[ci];
 #define C3_LAUNCH(BN_, MS_)                                                                                  \
     gemm_bf16_kernel<BN_, MS_><<<grid, kGemmThreads, GemmCfg<BN_, MS_>::kSmem, s>>>(                           \
-        ma, mb, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, sched, st)
+        ma, mb, mc, has_mc, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, sched, st)
     if (c.bn == 256 && c.msub == 1) C3_LAUNCH(256, 1);
     else if (c.bn == 128 && c.msub == 1) C3_LAUNCH(128, 1);
     else if (c.bn == 256 && c.msub == 2) C3_LAUNCH(256, 2);
@@ -457,12 +568,13 @@ static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap
 
 // Plans one GEMM: configuration, grid, tensor maps.
 struct GemmPlan {
-    int ci, grid, num_kb;
+    int ci, grid, num_kb, has_mc;
     int64_t num_m, num_n;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
 };
 
-static int plan_gemm(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int cap, GemmPlan* p) {
+static int plan_gemm(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int cap,
+                     GemmPlan* p) {
     p->ci = choose_cfg(M, N, K, cap);
     const TileCfg& c = kCfgs[p->ci];
     p->num_m = (M + 128LL * c.msub - 1) / (128LL * c.msub);
@@ -473,7 +585,11 @@ static int plan_gemm(const void* A, const void* B, int64_t M, int64_t N, int64_t
     p->num_kb = (int)((K + kBK - 1) / kBK);
     int rc = make_map(&p->ma, A, M, K, kBM);
     if (rc) return rc;
-    return make_map(&p->mb, B, N, K, c.bn);
+    if ((rc = make_map(&p->mb, B, N, K, c.bn))) return rc;
+    rc = make_out_map(&p->mc, C, M, N);
+    if (rc < 0) return rc;
+    p->has_mc = rc;
+    return 0;
 }
 
 int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,
@@ -492,7 +608,7 @@ int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, i
     if (!ds) return -3;
     const int cap = (sm_budget <= 0 || sm_budget > ds->sm_count) ? ds->sm_count : sm_budget;
     GemmPlan p;
-    int rc = plan_gemm(A, B, M, N, K, cap, &p);
+    int rc = plan_gemm(A, B, C, M, N, K, cap, &p);
     if (rc) return rc;
     g->kind = 2;
     g->ci = p.ci;
@@ -502,6 +618,8 @@ int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, i
     g->num_n = p.num_n;
     g->ma = p.ma;
     g->mb = p.mb;
+    g->mc = p.mc;
+    g->has_mc = p.has_mc;
     return 0;
 }
 
@@ -512,7 +630,8 @@ int gemm_enqueue(const GemmLaunch& g, cudaStream_t s, DevStatus* st, int* ctas_o
     DeviceState* ds = device_state();
     if (!ds) return -3;
     unsigned int* sched = st ? st->sched[ds->next_sched++ % kSchedSlots] : nullptr;
-    int rc = launch_cfg(g.ci, g.grid, g.ma, g.mb, g.C, g.M, g.N, g.num_m, g.num_n, g.num_kb, sched, st, s);
+    int rc = launch_cfg(g.ci, g.grid, g.ma, g.mb, g.mc, g.has_mc, g.C, g.M, g.N, g.num_m, g.num_n, g.num_kb, sched,
+                        st, s);
     if (rc) return rc;
     if (ctas_out) *ctas_out = g.grid;
     return 0;
@@ -617,15 +736,15 @@ extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M
         return e == cudaSuccess ? 0 : set_cuda_error(e, "cudaMemsetAsync");
     }
     GemmPlan plan;
-    if ((rc = plan_gemm(A, B, M, N, K, cap, &plan))) return rc;
+    if ((rc = plan_gemm(A, B, C, M, N, K, cap, &plan))) return rc;
     // The static block records at most kCtaRecs CTAs: refuse a launch that would need more.
     if (plan.grid > kCtaRecs)
         return set_error(-5, "c3_gemm_noalloc: more than 256 CTAs would need more than its 16 KiB scratch");
     // The block keeps the previous call's contents: clear it on this stream first.
     if ((rc = status_reset_launch(d->scratch, s))) return rc;
     unsigned int* sched = d->scratch->sched[d->next_sched++ % kSchedSlots];
-    if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, C, M, N, plan.num_m, plan.num_n, plan.num_kb,
-                         sched, d->scratch, s)))
+    if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, plan.mc, plan.has_mc, C, M, N, plan.num_m,
+                         plan.num_n, plan.num_kb, sched, d->scratch, s)))
         return rc;
     cudaError_t e;
     if (!check) return 0;
