@@ -127,6 +127,7 @@ struct GemmLaunch {
     int ci = 0, grid = 0, num_kb = 0;
     int64_t num_m = 0, num_n = 0;
     int has_mc = 0;  // mc (the fp32 output as a TMA store target) is valid: N % 4 == 0
+    int static_first = 1;  // CTA b starts on tile b; 0 when CTAs may start late (reclaim)
     CUtensorMap ma, mb, mc;
 };
 int gemm_prepare(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int sm_budget,

@@ -445,6 +445,8 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     const int gemm_cap = (!serial && sm_split > 0 && !reclaim_mode) ? ds.sm_count - sm_split : 0;
     GemmLaunch gl;
     if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, gemm_cap, &gl))) return rc;
+    // with reclaim, CTAs that find their SM held start late: every tile, the first included, is claimed
+    if (reclaim_mode) gl.static_first = 0;
     if ((e = cudaEventRecord(ev0, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     if (serial) {
         rc = gemm_enqueue(gl, s0, ds.status, &gctas);

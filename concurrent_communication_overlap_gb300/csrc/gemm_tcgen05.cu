@@ -105,7 +105,7 @@ template <int BN, int MSUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, int has_mc, float* __restrict__ C, int M, int N,
-                     int num_m, int num_n, int num_kb, unsigned int* sched, DevStatus* st) {
+                     int num_m, int num_n, int num_kb, unsigned int* sched, int static_first, DevStatus* st) {
     using Cfg = GemmCfg<BN, MSUB>;
     constexpr int S = Cfg::kStages;
     constexpr int NB = Cfg::kAccBufs;
@@ -171,12 +171,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // dealt round-robin when there is none), published to the other
             // roles through the tile ring, and the sentinel total_tiles ends
             // every role's loop.  A CTA that starts late (its SM was busy)
-            // simply claims fewer tiles.
+            // simply claims fewer tiles.  With static_first, CTA b starts on
+            // tile b without waiting for the counter (every CTA starts at
+            // once) and the counter hands out tiles from gridDim.x on.
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b = policy_evict_normal();
             int stage = 0;
             uint32_t phase = 0;
-            int t = sched ? (int)min(atomicAdd(&sched[0], 1u), (unsigned)total_tiles) : (int)blockIdx.x;
+            const unsigned claim_base = static_first ? gridDim.x : 0u;
+            int t = (sched && !static_first) ? (int)min(atomicAdd(&sched[0], 1u), (unsigned)total_tiles)
+                                             : (int)blockIdx.x;
             for (int i = 0;; ++i) {
                 const int slot = i & (kTR - 1);
                 if (!mbar_wait(bar(BAR_REMPTY + slot), ((uint32_t)(i / kTR) & 1u) ^ 1u, abort_flag)) {
@@ -186,8 +190,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tile_ring[slot] = t < total_tiles ? t : total_tiles;
                 mbar_arrive(bar(BAR_RFULL + slot));
                 if (t >= total_tiles) break;
-                const int next =
-                    sched ? (int)min(atomicAdd(&sched[0], 1u), (unsigned)total_tiles) : t + (int)gridDim.x;
+                // The next tile is claimed once this tile's first loads are in
+                // flight; its value is needed only after the last one.
+                unsigned next_raw = 0;
                 int mb, nb;
                 tile_coords(t, num_m, num_n, mb, nb);
                 bool ok = true;
@@ -202,13 +207,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int sub = 0; sub < MSUB; ++sub)
                         tma_load_2d(stage_a(stage, sub), &tmA, bar(stage), kb * kBK, mb * kRowsCta + sub * kBM, pol_a);
                     tma_load_2d(stage_b(stage), &tmB, bar(stage), kb * kBK, nb * BN, pol_b);
+                    if (kb == 0 && sched) next_raw = atomicAdd(&sched[0], 1u);
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                t = next;
+                t = sched ? (int)min(claim_base + next_raw, (unsigned)total_tiles) : t + (int)gridDim.x;
             }
             // The launch's last CTA to finish puts its scheduler slot back to zero.
             if (sched) {
@@ -549,11 +555,11 @@ static int choose_cfg(int64_t M, int64_t N, int64_t K, int cap) {
 
 static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                       int has_mc, float* C, int64_t M, int64_t N, int64_t num_m, int64_t num_n, int num_kb,
-                      unsigned int* sched, DevStatus* st, cudaStream_t s) {
+                      unsigned int* sched, int static_first, DevStatus* st, cudaStream_t s) {
     const TileCfg& c = kCfgs[ci];
 #define C3_LAUNCH(BN_, MS_)                                                                                  \
     gemm_bf16_kernel<BN_, MS_><<<grid, kGemmThreads, GemmCfg<BN_, MS_>::kSmem, s>>>(                           \
-        ma, mb, mc, has_mc, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, sched, st)
+        ma, mb, mc, has_mc, C, (int)M, (int)N, (int)num_m, (int)num_n, num_kb, sched, static_first, st)
     if (c.bn == 256 && c.msub == 1) C3_LAUNCH(256, 1);
     else if (c.bn == 128 && c.msub == 1) C3_LAUNCH(128, 1);
     else if (c.bn == 256 && c.msub == 2) C3_LAUNCH(256, 2);
@@ -631,7 +637,7 @@ int gemm_enqueue(const GemmLaunch& g, cudaStream_t s, DevStatus* st, int* ctas_o
     if (!ds) return -3;
     unsigned int* sched = st ? st->sched[ds->next_sched++ % kSchedSlots] : nullptr;
     int rc = launch_cfg(g.ci, g.grid, g.ma, g.mb, g.mc, g.has_mc, g.C, g.M, g.N, g.num_m, g.num_n, g.num_kb, sched,
-                        st, s);
+                        g.static_first, st, s);
     if (rc) return rc;
     if (ctas_out) *ctas_out = g.grid;
     return 0;
@@ -744,7 +750,7 @@ extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M
     if ((rc = status_reset_launch(d->scratch, s))) return rc;
     unsigned int* sched = d->scratch->sched[d->next_sched++ % kSchedSlots];
     if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, plan.mc, plan.has_mc, C, M, N, plan.num_m,
-                         plan.num_n, plan.num_kb, sched, d->scratch, s)))
+                         plan.num_n, plan.num_kb, sched, 1, d->scratch, s)))
         return rc;
     cudaError_t e;
     if (!check) return 0;
