@@ -92,8 +92,7 @@ struct DeviceState {
     int smem_per_sm = 0;
     int smem_per_block = 0;
     int cc_major = 0, cc_minor = 0;
-    cudaStream_t s_gemm = nullptr;     // default priority
-    cudaStream_t s_comm = nullptr;     // default priority
+    cudaStream_t s_comm = nullptr;     // the forked collective, default priority
     cudaStream_t s_comm_hi = nullptr;  // highest priority
     cudaStream_t s_capture = nullptr;  // private stream for capturing copy-engine graphs
     cudaEvent_t ev[8] = {};

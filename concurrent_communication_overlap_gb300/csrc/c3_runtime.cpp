@@ -67,7 +67,6 @@ static int init_device(DeviceState& ds, int dev) {
     if (ds.sm_count > 256) return set_error(C3_EUNSUP, "more than 256 SMs: %smid maps hold 256");
     int lo = 0, hi = 0;
     C3_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi), "stream priority range");
-    C3_TRY(cudaStreamCreateWithPriority(&ds.s_gemm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
     C3_TRY(cudaStreamCreateWithFlags(&ds.s_capture, cudaStreamNonBlocking), "stream");
@@ -84,7 +83,6 @@ static int init_device(DeviceState& ds, int dev) {
 }
 
 static void release_device(DeviceState& ds) {
-    if (ds.s_gemm) cudaStreamDestroy(ds.s_gemm);
     if (ds.s_comm) cudaStreamDestroy(ds.s_comm);
     if (ds.s_comm_hi) cudaStreamDestroy(ds.s_comm_hi);
     if (ds.s_capture) cudaStreamDestroy(ds.s_capture);
@@ -458,9 +456,11 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     } else {
         if (sm_split < 0 || sm_split >= ds.sm_count)
             return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
-        cudaStream_t sg = ds.s_gemm;
+        // The GEMM runs on the caller's stream and only the collective is
+        // forked onto a stream of its own: one cross-stream dependency on
+        // the way in and one on the way out, instead of two each.
+        cudaStream_t sg = s0;
         cudaStream_t sc = priority ? ds.s_comm_hi : ds.s_comm;
-        if ((e = cudaStreamWaitEvent(sg, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         const bool reclaim = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
         if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
@@ -479,7 +479,6 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         }
         if ((e = cudaEventRecord(ev_g, sg)) != cudaSuccess) return set_cuda_error(e, "event record");
         if ((e = cudaEventRecord(ev_c, sc)) != cudaSuccess) return set_cuda_error(e, "event record");
-        if ((e = cudaStreamWaitEvent(s0, ev_g, 0)) != cudaSuccess) return set_cuda_error(e, "join");
         if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
     }
     if ((e = cudaEventRecord(ev_end, s0)) != cudaSuccess) return set_cuda_error(e, "event record");

@@ -34,8 +34,10 @@
  *   - Streams are `cudaStream_t` values passed as `c3_stream` (void *); NULL
  *     means the legacy default stream.
  *   - The library owns a few internal objects per device, created on first use
- *     with that device current and released by c3_shutdown(): two CUDA streams
- *     (one at the highest priority), CUDA events, a 16 KiB device status block
+ *     with that device current and released by c3_shutdown(): three CUDA
+ *     streams (the forked collective's, the same at the highest priority, and
+ *     a private stream for capturing memcpy graphs), CUDA events, up to 16
+ *     cached memcpy graphs, a 16 KiB device status block
  *     (error word, %globaltimer stamps, per-CTA %smid residency records) and
  *     the kernels' function attributes.
  *   - Return value: C3_OK (0) or a negative c3_status.  On an argument error
@@ -290,8 +292,11 @@ typedef struct {
  *                    CTA fits beside them) and the GEMM on the others.
  *     priority == 1: schedule prioritisation -- the collective is launched
  *                    first, on the library's highest-priority stream; 0: the
- *                    GEMM is launched first and both streams have default
- *                    priority.  (Pages: c3_sp, c3_rp and their combination.)
+ *                    GEMM is launched first and the collective's stream has
+ *                    default priority.  (Pages: c3_sp, c3_rp and their
+ *                    combination.)
+ *   In every concurrent mode the GEMM runs on p->stream and the collective on
+ *   a library stream forked from it by an event and joined back by another.
  *   mode C3_MODE_CONCURRENT_CE: the collective as driver memcpy transfers on
  *     its own stream (ConCCL); sm_split > 0 removes that many SMs from the GEMM
  *     (ConCCL_rp).  priority as above.  (Device-to-device copies run on SMs
