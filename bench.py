@@ -893,81 +893,85 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
 
 def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out, prob, modes, best, dev,
                 stream, args):
-    """The same metric end to end through the public API with host buffers:
-    each phase copies its inputs from pinned host memory (A for the GEMM, the
-    shards / send buffer for the collective) and the GEMM phases read C back.
-    T_g = H2D(A) + c3_gemm + D2H(C); T_c = H2D(payload) + the collective on the
-    best mode's engine; T_conc = H2D(A, payload) + c3_run(best mode) + D2H(C)."""
+    """The same metric end to end through the public API with the step's
+    inputs in pinned host memory.  The GEMM chain copies A in, runs c3_gemm
+    and reads C back; the collective reads its sources straight from the
+    pinned host buffers (c3_allgather / c3_alltoall accept page-locked host
+    sources; the all-reduce, whose reduction needs device inputs, copies them
+    in first).  T_g = the GEMM chain alone, T_c = the collective alone, T_conc
+    = both chains at once on two streams, the collective on the best mode's
+    engine and, if that mode is prioritised, on a high-priority stream.  Both
+    calls use their default SM budgets: a partitioned mode's split is not
+    applied here."""
     name, mode, split, prio = next(m for m in modes if m[0] == best)
     engine = c3.C3_ENGINE_CE if mode in (2, 3) else c3.C3_ENGINE_SM
     hA = torch.from_numpy(A_h.view(np.int16)).pin_memory()
-    if dshards is not None:
-        hpay = [torch.from_numpy(s).pin_memory() for s in payload]
-        dpay = dshards
-    else:
+    if w.coll == "alltoall":
         hpay = [torch.from_numpy(payload).pin_memory()]
-        dpay = [dsend]
+    else:
+        hpay = [torch.from_numpy(s).pin_memory() for s in payload]
     hC = torch.empty(dC.shape, dtype=torch.float32).pin_memory()
     bi_a = hA.numel() * 2
     bi_p = sum(h.numel() * h.element_size() for h in hpay)
     bo = hC.numel() * 4
+    s2 = torch.cuda.Stream(dev, priority=-1 if prio else 0)  # -1: a higher priority than the default 0
 
-    def h2d_a():
-        dA.copy_(hA, non_blocking=True)
+    def gemm_chain(s):
+        with torch.cuda.stream(s):
+            dA.copy_(hA, non_blocking=True)
+            c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, s)
+            hC.copy_(dC, non_blocking=True)
 
-    def h2d_p():
-        for d, h in zip(dpay, hpay):
-            d.copy_(h, non_blocking=True)
-
-    def d2h_c():
-        hC.copy_(dC, non_blocking=True)
-
-    def coll():
-        if w.coll == "allreduce":
-            c3.c3_allreduce(dshards, out, w.unit_bytes // 4, w.nranks, engine=engine, stream=stream)
-        elif dshards is not None:
-            c3.c3_allgather(dshards, out, w.unit_bytes, w.nranks, engine=engine, stream=stream)
+    def coll_chain(s):
+        if w.coll == "allgather":
+            c3.c3_allgather(hpay, out, w.unit_bytes, w.nranks, engine=engine, stream=s)
+        elif w.coll == "alltoall":
+            c3.c3_alltoall(hpay[0], out, w.unit_bytes, w.nranks, engine=engine, stream=s)
         else:
-            c3.c3_alltoall(dsend, out, w.unit_bytes, w.nranks, engine=engine, stream=stream)
-
-    def gemm_phase():
-        h2d_a()
-        c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
-        d2h_c()
-
-    def coll_phase():
-        h2d_p()
-        coll()
-
-    def conc_phase():
-        h2d_a()
-        h2d_p()
-        c3.c3_run(prob, mode, split, prio)
-        d2h_c()
+            with torch.cuda.stream(s):
+                for d, h in zip(dshards, hpay):
+                    d.copy_(h, non_blocking=True)
+            c3.c3_allreduce(dshards, out, w.unit_bytes // 4, w.nranks, engine=engine, stream=s)
 
     def timed(fn):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(stream)
-        fn()
+        fn(e0)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e-3
 
+    def conc(e0):
+        s2.wait_event(e0)
+        if prio:
+            coll_chain(s2)
+            gemm_chain(stream)
+        else:
+            gemm_chain(stream)
+            coll_chain(s2)
+        done = torch.cuda.Event()
+        done.record(s2)
+        stream.wait_event(done)
+
     recs = []
     for it in range(args.warmup + args.steps):
-        tg = timed(gemm_phase)
-        tc = timed(coll_phase)
-        tconc = timed(conc_phase)
+        tg = timed(lambda e0: gemm_chain(stream))
+        tc = timed(lambda e0: coll_chain(stream))
+        tconc = timed(conc)
         if it >= args.warmup:
             recs.append((tg, tc, tconc))
+    c3.c3_status_check(stream)
     tg = statistics.median(r[0] for r in recs)
     tc = statistics.median(r[1] for r in recs)
     tconc = statistics.median(r[2] for r in recs)
     m = pct_gain(tg, tc, tconc)
     return {"value": m["pct_ideal_gain"], "unit": UNIT, "h2d_bytes_per_step": 2 * (bi_a + bi_p),
             "d2h_bytes_per_step": 2 * bo, "mode": best, "t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc,
-            "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"]}
+            "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"],
+            "engine": "memcpy" if engine == c3.C3_ENGINE_CE else "sm",
+            "collective_sources": ("copied to HBM first (the reduction needs device inputs)" if w.coll == "allreduce"
+                                   else "pinned host memory, read by the collective itself")}
 
 
 if __name__ == "__main__":
