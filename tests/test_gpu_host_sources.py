@@ -1,4 +1,5 @@
-"""GPU parity of collectives whose sources sit in page-locked host memory.
+"""GPU parity of collectives whose sources sit in page-locked host memory,
+alone, in every c3_run mode, and as asynchronous calls beside the GEMM.
 
 The remote ranks' buffers are placed across the CPU-GPU link (pinned host
 memory) while the output stays in device memory.  The SM copy kernel reads
@@ -131,3 +132,48 @@ def test_host_source_argument_errors(c3):
     c3.c3_allgather(hs, out, sb, 8)
     c3.c3_status_check()
     assert np.array_equal(out.cpu().numpy(), oracle.allgather(shards))
+
+
+@pytest.mark.parametrize("engine", [0, 1])
+@pytest.mark.parametrize("coll", ["allgather", "alltoall"])
+def test_async_calls_on_two_streams(c3, engine, coll):
+    # What a caller with host-resident inputs does: the GEMM chain on one
+    # stream (copy A in, c3_gemm, read C back) and the collective reading its
+    # pinned host sources on another, both in flight at once.
+    w = I.WORKLOADS["tiny_ag"]
+    A, B = I.gemm_operands(w)
+    C_ref, S_ref = oracle.gemm(A, B)
+    hA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16)).pin_memory()
+    dA = torch.empty(hA.shape, dtype=torch.int16, device="cuda")
+    dB = dev_u16(B)
+    dC = torch.full((w.M, w.N), float("nan"), device="cuda")
+    hC = torch.empty((w.M, w.N), dtype=torch.float32).pin_memory()
+    unit = 1 << 20 if coll == "allgather" else 128 * 1024
+    if coll == "allgather":
+        payload = [I.random_bytes(1002 + r, unit) for r in range(8)]
+        ref = oracle.allgather(payload)
+        srcs = [pinned_bytes(x) for x in payload]
+    else:
+        payload = I.random_bytes(1002, 64 * unit)
+        ref = oracle.alltoall(payload, 8)
+        srcs = pinned_bytes(payload)
+    out = torch.zeros(ref.size, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        dC.fill_(float("nan"))
+        out.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s1):
+            dA.copy_(hA, non_blocking=True)
+            c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, s1)
+            hC.copy_(dC, non_blocking=True)
+        if coll == "allgather":
+            c3.c3_allgather(srcs, out, unit, 8, engine=engine, stream=s2)
+        else:
+            c3.c3_alltoall(srcs, out, unit, 8, engine=engine, stream=s2)
+        torch.cuda.synchronize()
+        c3.c3_status_check()
+        assert np.array_equal(out.cpu().numpy(), ref)
+        C = hC.numpy().astype(np.float64)
+        assert not np.isnan(C).any()
+        assert (np.abs(C - C_ref) <= 1e-4 * S_ref).all()
