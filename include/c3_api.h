@@ -260,7 +260,8 @@ typedef struct {
     double t_comm_iso;     /* collective alone on the engine the mode uses           (c3_time) */
     double t_serial;       /* t_gemm_iso + t_comm_iso: the serial time               (c3_time) */
     double t_serial_meas;  /* GEMM then collective on one stream, measured           (c3_time) */
-    double t_conc;         /* fork to join of the requested mode                     (c3_run)  */
+    double t_conc;         /* start event to the later of the GEMM's and the collective's
+                              completion events (events recorded right after each)  (c3_run)  */
     double t_ideal;        /* max(t_gemm_iso, t_comm_iso)                            (c3_time) */
     double s_ideal;        /* t_serial / t_ideal                                     (c3_time) */
     double s_real;         /* t_serial / t_conc                                      (c3_time) */

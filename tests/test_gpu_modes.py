@@ -83,6 +83,9 @@ def test_mode_runs_and_outputs_are_exact(c3, setup, name, mode, split, prio):
     setup.poison()
     t = c3.c3_run(setup.p, mode, split, prio)
     assert t["status"] == 0 and t["t_conc"] > 0
+    # T_conc runs from the start event to the later of the two completion events
+    assert t["t_gemm_ev"] > 0 and t["t_comm_ev"] > 0
+    assert t["t_conc"] == max(t["t_gemm_ev"], t["t_comm_ev"])
     assert t["gemm_ctas"] >= 1
     if mode in (2, 3):  # memcpy path: no collective kernel of this library ran
         assert t["comm_ctas"] == 0 and t["comm_sms"] == 0
