@@ -721,6 +721,18 @@ def main(argv=None):
     gemm_ok = gemm_rows_ok(np, A_h, B_h, rows, Cg)
 
     # ---- statistics per mode (medians over the timed steps)
+    peaks = load_peaks()
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    gemm_hbm_bound = w.gemm_flops / w.gemm_bytes < ridge
+
+    def gemm_frac(t):
+        """The GEMM's roofline fraction over a window of t seconds."""
+        if not t or t <= 0:
+            return None
+        if gemm_hbm_bound:
+            return w.gemm_bytes / t / 1e9 / peaks["hbm_gbs"]
+        return w.gemm_flops / t / 1e12 / peaks["bf16_tflops"]
+
     stats = {}
     all_tg = [r["t_gemm_iso"] for recs in per_mode.values() for r in recs]
     tc_strict = strict_comm_time(per_mode, modes)
@@ -748,6 +760,12 @@ def main(argv=None):
             "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / statistics.median(tcd) / 1e9
                                  if statistics.median(tcd) > 0 else None),
             "gemm_slowdown": tgd / tg if tg > 0 else None,
+            # roofline fractions: the GEMM against HBM or the tensor peak (whichever bounds it),
+            # isolated (event time) and under overlap (its device window); the SM copy against HBM
+            "gemm_roofline_frac_iso": gemm_frac(tg),
+            "gemm_roofline_frac_overlap": gemm_frac(tgd),
+            "copy_roofline_frac_overlap": (w.coll_traffic_bytes / statistics.median(tcd) / 1e9 / peaks["hbm_gbs"]
+                                           if statistics.median(tcd) > 0 and not host_src else None),
             "gemm_ctas": recs[0]["gemm_ctas"], "comm_ctas": recs[0]["comm_ctas"],
             "smid_overlap_max": max(r["smid_overlap"] for r in recs),
         }
@@ -755,7 +773,6 @@ def main(argv=None):
     value = reduce_mean(pg, stats[best]["pct_ideal_gain"], dev)
 
     # ---- roofline of the dominant kernel (the GEMM; bytes-bound on this workload)
-    peaks = load_peaks()
     tg_mean = statistics.fmean(all_tg)
     flops_ai = w.gemm_flops / w.gemm_bytes
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
