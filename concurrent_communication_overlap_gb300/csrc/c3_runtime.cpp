@@ -19,6 +19,8 @@
 #include "../../include/c3_api.h"
 #include "c3_internal.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <chrono>
 #include <cstdio>
@@ -427,8 +429,30 @@ static int check_problem(const c3_problem* p, CollPlan* cp) {
 
 // One run of `mode` on already-checked arguments; fills t_conc, the event
 // times and the device facts.
+// NVTX range around one timed phase, so that a profiler can select or filter
+// the kernels each phase launches (ncu --nvtx, nsys); free when no tool is attached.
+struct PhaseRange {
+    explicit PhaseRange(const char* name) { nvtxRangePushA(name); }
+    ~PhaseRange() { nvtxRangePop(); }
+    PhaseRange(const PhaseRange&) = delete;
+    PhaseRange& operator=(const PhaseRange&) = delete;
+};
+
+static const char* mode_range_name(int mode, int sm_split, int priority) {
+    switch (mode) {
+        case C3_MODE_SERIAL_SM: return "c3/serial (SM collective)";
+        case C3_MODE_SERIAL_CE: return "c3/serial (memcpy collective)";
+        case C3_MODE_CONCURRENT_CE: return sm_split ? "c3/concurrent memcpy, GEMM capped" : "c3/concurrent memcpy";
+        case C3_MODE_CONCURRENT_SM_RECLAIM: return "c3/concurrent SM, partition with reclaim";
+        default:
+            if (sm_split) return priority ? "c3/concurrent SM, prioritised + partitioned" : "c3/concurrent SM, partitioned";
+            return priority ? "c3/concurrent SM, prioritised" : "c3/concurrent SM, baseline";
+    }
+}
+
 static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int mode, int sm_split,
                     int priority, c3_timing* out) {
+    PhaseRange range(mode_range_name(mode, sm_split, priority));
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
     cudaEvent_t ev0 = ds.ev[0], ev_g = ds.ev[1], ev_c = ds.ev[2], ev_end = ds.ev[3];
     int rc = status_reset_launch(ds.status, s0);
@@ -496,7 +520,8 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
 
 // Times one phase that runs entirely on `s0`: fn() enqueues it.
 template <class F>
-static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, double* t_out, F fn) {
+static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, const char* name, double* t_out, F fn) {
+    PhaseRange range(name);
     int rc;
     if (p->flush_buf && p->flush_bytes && (rc = l2_flush_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
     cudaError_t e;
@@ -720,13 +745,14 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
         std::memset(&r, 0, sizeof r);
         GemmLaunch gl;
         if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, 0, &gl))) return rc;
-        rc = time_phase(*ds, s0, p, &r.t_gemm_iso, [&] { return gemm_enqueue(gl, s0, ds->status, nullptr); });
+        rc = time_phase(*ds, s0, p, "c3/GEMM alone", &r.t_gemm_iso,
+                        [&] { return gemm_enqueue(gl, s0, ds->status, nullptr); });
         if (rc) return rc;
-        rc = time_phase(*ds, s0, p, &r.t_comm_iso, [&] {
+        rc = time_phase(*ds, s0, p, "c3/collective alone", &r.t_comm_iso, [&] {
             return launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
-        rc = time_phase(*ds, s0, p, &r.t_serial_meas, [&] {
+        rc = time_phase(*ds, s0, p, "c3/GEMM then collective", &r.t_serial_meas, [&] {
             int r1 = gemm_enqueue(gl, s0, ds->status, nullptr);
             return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
