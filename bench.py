@@ -141,14 +141,19 @@ def expected_collective(np, w, payload):
     return np.tile(acc, len(payload)).view(np.uint8)
 
 
-def gemm_rows_ok(np, A_bits, B_bits, rows, C_rows):
-    """Sampled GEMM rows within |C - exact| <= 1e-4 * sum_k |a b|: the bf16
-    operands widened exactly, products and sums in fp64 (numpy)."""
+def gemm_rows_reference(np, A_bits, B_bits, rows):
+    """Exact values and tolerances of sampled GEMM rows: the bf16 operands
+    widened exactly, products and sums in fp64 (numpy); the tolerance is
+    1e-4 * sum_k |a b|."""
     def widen(u16):
         return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     A, B = widen(A_bits[rows]), widen(B_bits)
-    ref = A @ B.T
-    bound = 1e-4 * (np.abs(A) @ np.abs(B).T)
+    return A @ B.T, 1e-4 * (np.abs(A) @ np.abs(B).T)
+
+
+def gemm_rows_ok(np, A_bits, B_bits, rows, C_rows, reference=None):
+    """Sampled GEMM rows within their tolerance (see gemm_rows_reference)."""
+    ref, bound = reference if reference is not None else gemm_rows_reference(np, A_bits, B_bits, rows)
     C = np.asarray(C_rows, dtype=np.float64)
     return bool(np.isfinite(C).all() and (np.abs(C - ref) <= bound).all())
 
@@ -714,11 +719,26 @@ def main(argv=None):
     ms_per_step = ev0.elapsed_time(ev1) / args.steps
     ms_per_step = reduce_max(pg, ms_per_step, dev)
 
-    # ---- post-run validation (every mode ran on these buffers; check the last outputs)
-    coll_ok = bool(np.array_equal(out.cpu().numpy().view(np.uint8), expected_collective(np, w, payload)))
+    # ---- post-run validation: the outputs of the timed steps, then every mode once more on
+    # poisoned buffers (untimed), each checked against the definitions
+    expected = expected_collective(np, w, payload)
     rows = np.array([0, 1, w.M // 2, w.M - 1])
-    Cg = dC[torch.from_numpy(rows).to(dev)].cpu().numpy()
-    gemm_ok = gemm_rows_ok(np, A_h, B_h, rows, Cg)
+    rows_ref = gemm_rows_reference(np, A_h, B_h, rows)
+    rows_dev = torch.from_numpy(rows).to(dev)
+
+    def outputs_ok():
+        c_ok = bool(np.array_equal(out.cpu().numpy().view(np.uint8), expected))
+        g_ok = gemm_rows_ok(np, A_h, B_h, rows, dC[rows_dev].cpu().numpy(), rows_ref)
+        return c_ok, g_ok
+
+    coll_ok, gemm_ok = outputs_ok()
+    per_mode_ok = {}
+    for name, mode, split, prio in modes:
+        out.fill_(0xA5)
+        dC.fill_(float("nan"))
+        c3.c3_run(prob, mode, split, prio)
+        per_mode_ok[name] = outputs_ok()
+    torch.cuda.synchronize(dev)
 
     # ---- statistics per mode (medians over the timed steps)
     peaks = load_peaks()
@@ -821,7 +841,11 @@ def main(argv=None):
         "copy_gbs_overlap": stats[best]["copy_gbs_overlap"],
         "roofline": roof, "roofline_copy": copy_roof,
         "gpu_launches": launches,
-        "validation": {"collective_bit_exact": coll_ok, "gemm_rows_in_tolerance": gemm_ok},
+        "validation": {"collective_bit_exact": coll_ok and all(v[0] for v in per_mode_ok.values()),
+                       "gemm_rows_in_tolerance": gemm_ok and all(v[1] for v in per_mode_ok.values()),
+                       "per_mode": {k: {"collective_bit_exact": v[0], "gemm_rows_in_tolerance": v[1]}
+                                    for k, v in per_mode_ok.items()},
+                       "gemm_rows": [int(r) for r in rows]},
         "modes": stats,
         "device": {"name": torch.cuda.get_device_name(dev), **info},
     }

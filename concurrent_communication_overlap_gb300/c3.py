@@ -24,6 +24,7 @@ C3_MODE_CONCURRENT_SM_RECLAIM = 4
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
 C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH, C3_CE_GRAPH_PARALLEL = 0, 1, 2, 3
+C3_FAULT_NONE, C3_FAULT_GEMM_LAUNCH, C3_FAULT_SM_COLL_LAUNCH, C3_FAULT_MEMCPY, C3_FAULT_DEVICE_INIT = 0, 1, 2, 3, 4
 CLASS_NAMES = {0: "G-long", 1: "GC-equal", 2: "C-long"}
 
 _i64, _int, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
@@ -93,6 +94,7 @@ def _load():
         "c3_l2_flush": [_vp, _sz, _vp],
         "c3_gemm_noalloc": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _int],
         "c3_selftest_wait": [ctypes.c_uint64, _int, _vp],
+        "c3_inject_fault": [_int],
         "c3_sp_predict": [_int, _int],
         "c3_rp_predict": [ctypes.POINTER(C3RpTable), ctypes.c_double, ctypes.c_double, ctypes.c_double,
                           ctypes.c_double, ctypes.c_double, ctypes.POINTER(_int), ctypes.POINTER(ctypes.c_double),
@@ -113,7 +115,8 @@ def _load():
 _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_allreduce", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
-            "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_sp_predict", "c3_rp_predict")
+            "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_inject_fault", "c3_sp_predict",
+            "c3_rp_predict")
 
 
 def lib():
@@ -207,6 +210,11 @@ def c3_gemm_plan(M, N, K, sm_budget=0):
 def c3_selftest_wait(limit_ns, arrive, stream=None):
     """Status of a bounded device wait that succeeds (arrive=1) or runs out (arrive=0)."""
     return int(_lib.c3_selftest_wait(int(limit_ns), int(arrive), _stream(stream)))
+
+
+def c3_inject_fault(site):
+    """Arm a one-shot host-side failure at `site` (C3_FAULT_*; NONE disarms)."""
+    _check(_lib.c3_inject_fault(int(site)), "c3_inject_fault")
 
 
 def c3_sp_predict(gemm_ctas, coll_ctas):

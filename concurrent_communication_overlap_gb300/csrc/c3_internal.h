@@ -145,6 +145,11 @@ int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStre
 int bulk_copy_smem_bytes();
 
 int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream);
+
+// One-shot host-side failure injection (c3_inject_fault): true, and disarmed,
+// when `site` is the armed site.  Site values are those of c3_fault_site.
+enum { kFaultGemmLaunch = 1, kFaultSmCollLaunch = 2, kFaultMemcpy = 3, kFaultDeviceInit = 4 };
+bool take_fault(int site);
 void ce_release_graphs(int device);
 
 int status_reset_launch(DevStatus* st, cudaStream_t s);

@@ -45,6 +45,17 @@ int set_error(int code, const char* what) {
     return code;
 }
 
+static std::atomic<int> g_fault{0};
+
+bool take_fault(int site) {
+    int armed = site;
+    return site != 0 && g_fault.compare_exchange_strong(armed, 0);
+}
+
+static_assert(kFaultGemmLaunch == C3_FAULT_GEMM_LAUNCH && kFaultSmCollLaunch == C3_FAULT_SM_COLL_LAUNCH &&
+                  kFaultMemcpy == C3_FAULT_MEMCPY && kFaultDeviceInit == C3_FAULT_DEVICE_INIT,
+              "fault site values");
+
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
 
@@ -73,6 +84,8 @@ static int init_device(DeviceState& ds, int dev) {
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
     C3_TRY(cudaStreamCreateWithFlags(&ds.s_capture, cudaStreamNonBlocking), "stream");
     for (auto& ev : ds.ev) C3_TRY(cudaEventCreate(&ev), "event");
+    if (take_fault(kFaultDeviceInit))
+        return set_error(C3_ECUDA, "injected failure: device initialisation (status block allocation refused)");
     C3_TRY(cudaMalloc(reinterpret_cast<void**>(&ds.status), kStatusBytes), "status block");
     C3_TRY(cudaMemset(ds.status, 0, kStatusBytes), "status block");
 #undef C3_TRY
@@ -660,6 +673,12 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     if (!ds) return C3_ECUDA;
     if ((rc = locate_plan(*ds, &t))) return rc;
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+}
+
+int c3_inject_fault(int site) {
+    if (site < C3_FAULT_NONE || site > C3_FAULT_DEVICE_INIT) return set_error(C3_EINVAL, "unknown fault site");
+    g_fault.store(site);
+    return C3_OK;
 }
 
 int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s) {

@@ -182,6 +182,7 @@ static int ce_graph(const SegTable& t, bool parallel, cudaStream_t s, cudaStream
 
 int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream) {
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
+    if (take_fault(kFaultMemcpy)) return set_error(-3, "injected failure: memcpy transfer");
     if (variant == kCeStrided) return ce_strided(t, s);
     if (variant == kCeGraph) return ce_graph(t, false, s, capture_stream);
     if (variant == kCeGraphParallel) return ce_graph(t, true, s, capture_stream);

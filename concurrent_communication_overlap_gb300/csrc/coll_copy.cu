@@ -220,6 +220,7 @@ int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStre
                           int* ctas_out) {
     if (ctas_out) *ctas_out = 0;
     if (t.count == 0) return 0;
+    if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) ctas = 1;
     reduce_scatter_kernel<<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
     cudaError_t e = cudaGetLastError();
@@ -251,6 +252,7 @@ int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, i
                    DevStatus* st, int* ctas_out) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
+    if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) ctas = 1;
     if (flavour == kSmkBulk) {
         if (l2_stream)

@@ -556,6 +556,7 @@ static int choose_cfg(int64_t M, int64_t N, int64_t K, int cap) {
 static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                       int has_mc, float* C, int64_t M, int64_t N, int64_t num_m, int64_t num_n, int num_kb,
                       unsigned int* sched, int static_first, DevStatus* st, cudaStream_t s) {
+    if (take_fault(kFaultGemmLaunch)) return set_error(-3, "injected failure: GEMM launch");
     const TileCfg& c = kCfgs[ci];
 #define C3_LAUNCH(BN_, MS_)                                                                                  \
     gemm_bf16_kernel<BN_, MS_><<<grid, kGemmThreads, GemmCfg<BN_, MS_>::kSmem, s>>>(                           \

@@ -372,6 +372,30 @@ int c3_gemm_noalloc(const void *A, const void *B, float *C, int64_t M, int64_t N
 int c3_selftest_wait(uint64_t limit_ns, int arrive, c3_stream s);
 
 /*
+ * Host-side failure injection, so that a caller's error paths (and this
+ * library's own recovery) can be tested without faulting a GPU.  Arms a
+ * one-shot failure of the next call, on any thread, that reaches `site`:
+ *   C3_FAULT_GEMM_LAUNCH     the GEMM kernel launch
+ *   C3_FAULT_SM_COLL_LAUNCH  an SM collective kernel launch (copy or reduce-scatter)
+ *   C3_FAULT_MEMCPY          the memcpy path's transfer calls
+ *   C3_FAULT_DEVICE_INIT     the per-device initialisation (as if allocating the
+ *                            status block were refused; takes effect on the next
+ *                            initialisation, i.e. after c3_shutdown)
+ * That step then launches nothing and returns C3_ECUDA, with c3_last_error()
+ * naming the injection; work enqueued before it in the same call stays
+ * enqueued.  C3_FAULT_NONE disarms.  Returns C3_OK, or C3_EINVAL for an
+ * unknown site.  The pages have no counterpart.
+ */
+typedef enum {
+    C3_FAULT_NONE = 0,
+    C3_FAULT_GEMM_LAUNCH = 1,
+    C3_FAULT_SM_COLL_LAUNCH = 2,
+    C3_FAULT_MEMCPY = 3,
+    C3_FAULT_DEVICE_INIT = 4
+} c3_fault_site;
+int c3_inject_fault(int site);
+
+/*
  * Runtime heuristics of the pages (Section V-C).
  *
  * c3_sp_predict: schedule prioritisation -- returns 1 when the collective

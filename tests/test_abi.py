@@ -109,6 +109,10 @@ def test_argument_errors_before_any_cuda_call(c3):
     assert c3.c3_selftest_wait(1000, 2) == c3.C3_EINVAL
     assert c3.lib().c3_l2_flush(0x1001, 64, None) == c3.C3_EALIGN
     assert c3.lib().c3_l2_flush(None, 64, None) == c3.C3_EINVAL
+    assert c3.lib().c3_inject_fault(5) == c3.C3_EINVAL
+    assert c3.lib().c3_inject_fault(-1) == c3.C3_EINVAL
+    assert c3.lib().c3_inject_fault(c3.C3_FAULT_GEMM_LAUNCH) == c3.C3_OK
+    assert c3.lib().c3_inject_fault(c3.C3_FAULT_NONE) == c3.C3_OK   # disarmed again
 
 
 def test_run_and_time_reject_bad_records(c3):

@@ -73,21 +73,16 @@ def test_gemm_matches_oracle(c3, M, N, K, budget, plan):
     assert_gemm_close(C, C_ref, S_ref)
 
 
-def test_gemm_full_size_memory_bound_sampled(c3):
+def test_gemm_full_size_memory_bound_every_entry(c3):
     # The bench workload in the bench's launch configuration: 256 x 28672 x 8192,
-    # N(0,1) activations, N(0,0.02) weights, every SM.  Checked on 6 full rows
-    # (every column, every tile) and 512 random entries against the oracle.
+    # N(0,1) activations, N(0,0.02) weights, every SM.  Every one of the 7.3 M
+    # outputs is checked against the oracle (fp64, multi-threaded on the host).
     w = I.WORKLOADS["mem_ag"]
     assert c3.c3_gemm_plan(w.M, w.N, w.K, 0)[:2] == (192, 2)
     A, B = I.gemm_operands(w)
     C = run_gemm(c3, A, B, 0)
-    rows = np.array([0, 1, 127, 128, 200, 255])
-    C_ref, S_ref = oracle.gemm(A[rows], B)
-    assert_gemm_close(C[rows], C_ref, S_ref)
-    rng = np.random.default_rng(5)
-    mi, ni = rng.integers(0, w.M, 512), rng.integers(0, w.N, 512)
-    c_ref, s_ref = oracle.gemm_entries(A, B, mi, ni)
-    assert_gemm_close(C[mi, ni], c_ref, s_ref)
+    C_ref, S_ref = oracle.gemm(A, B)
+    assert_gemm_close(C, C_ref, S_ref)
 
 
 def test_gemm_k_zero_writes_zeros(c3):
