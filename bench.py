@@ -461,8 +461,10 @@ def ce_variant_arg(args, c3):
 def run_sweep(args, c3, torch, np, I, dev, info):
     """The pages' size sweep: an 8192^3 GEMM against collectives of 1 MiB to
     1 GiB total (x2 steps), every mode of --modes (default: baseline,
-    prioritised, partitioned_32, ce), one JSON line per size."""
-    names = args.modes.split(",") if args.modes else ["baseline", "prioritised", "partitioned_32", "reclaim_16", "ce"]
+    prioritised, partitioned_32, partitioned_64, reclaim_16, ce), one JSON line
+    per size."""
+    names = (args.modes.split(",") if args.modes
+             else ["baseline", "prioritised", "partitioned_32", "partitioned_64", "reclaim_16", "ce"])
     modes = [m for m in MODES if m[0] in names]
     if args.sweep_max_mib < 1 or args.sweep_max_mib & (args.sweep_max_mib - 1):
         raise SystemExit("--sweep-max-mib must be a power of two")
