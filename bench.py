@@ -96,8 +96,9 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", choices=["allgather", "alltoall"], default=None,
                     help="instead of the headline line: one line per collective size (8192^3 GEMM, 1 MiB..1 GiB)")
     ap.add_argument("--sweep-max-mib", type=int, default=1024,
-                    help="largest collective total of the sweep, MiB (power of two; above 1024 extends the pages' "
-                         "range so that the device-resident sweep also reaches GC-equal and C-long pairs)")
+                    help="largest collective total of the sweep (and of --heuristics' scenarios), MiB (power of "
+                         "two; above 1024 extends the pages' range so that the device-resident sweep also reaches "
+                         "GC-equal and C-long pairs)")
     return ap.parse_args(argv)
 
 
@@ -576,7 +577,8 @@ def run_heuristics(args, c3, torch, np, I, dev, info):
     table = [(k, slow["compute"][i], slow["memory"][i], slow["coll"][i]) for i, k in enumerate(ks)]
 
     # ---- scenarios: the size sweep (both collectives) and the memory-bound workload
-    scen = [(w.name, w) for coll in ("allgather", "alltoall") for w in I.sweep_workloads(coll)]
+    scen = [(w.name, w) for coll in ("allgather", "alltoall")
+            for w in I.sweep_workloads(coll, hi_bytes=args.sweep_max_mib << 20)]
     scen.append(("mem_ag", I.WORKLOADS["mem_ag"]))
     rows, hits = [], 0
     cache = {}
