@@ -70,7 +70,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="a named workload, or a size-sweep point such as sweep_allgather_4194304k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
@@ -157,6 +158,18 @@ def gemm_rows_ok(np, A_bits, B_bits, rows, C_rows, reference=None):
     ref, bound = reference if reference is not None else gemm_rows_reference(np, A_bits, B_bits, rows)
     C = np.asarray(C_rows, dtype=np.float64)
     return bool(np.isfinite(C).all() and (np.abs(C - ref) <= bound).all())
+
+
+def find_workload(I, name):
+    """A named workload, or one of the size sweep's (sweep_<coll>_<KiB>k, up to 8 GiB)."""
+    if name in I.WORKLOADS:
+        return I.WORKLOADS[name]
+    for coll in ("allgather", "alltoall"):
+        for w in I.sweep_workloads(coll, hi_bytes=8 << 30):
+            if w.name == name:
+                return w
+    raise SystemExit(f"unknown workload {name!r}: one of {sorted(I.WORKLOADS)} or a sweep name such as "
+                     f"sweep_allgather_4194304k")
 
 
 def c3_class(tg, tc):
@@ -425,7 +438,7 @@ def run_reference(args, world, rank, pg):
     from concurrent_communication_overlap_gb300 import inputs as I
     if rank != 0:
         return 0
-    w = I.WORKLOADS[args.workload]
+    w = find_workload(I, args.workload)
     t0 = time.perf_counter()
     # size the sample so that the whole run (3 oracle GEMM phases per step)
     # stays near a minute, whatever --steps asks for
@@ -639,7 +652,7 @@ def main(argv=None):
         return run_sweep(args, c3, torch, np, I, dev, info)
     if args.heuristics:
         return run_heuristics(args, c3, torch, np, I, dev, info)
-    w = I.WORKLOADS[args.workload]
+    w = find_workload(I, args.workload)
     modes = MODES if not args.modes else [m for m in MODES if m[0] in args.modes.split(",")]
 
     # ---- inputs (host-generated, seeded), resident in HBM before timing
