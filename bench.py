@@ -957,12 +957,12 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
     pinned host buffers (c3_allgather / c3_alltoall accept page-locked host
     sources; the all-reduce, whose reduction needs device inputs, copies them
     in first).  T_g = the GEMM chain alone, T_c = the collective alone, T_conc
-    = both chains at once on two streams, the collective on the best mode's
-    engine and, if that mode is prioritised, on a high-priority stream.  Both
-    calls use their default SM budgets: a partitioned mode's split is not
-    applied here."""
+    = both chains at once on two streams (the collective's on a high-priority
+    stream if the best device mode is prioritised).  Both engines are
+    measured; as on the device side, the ideal uses the faster engine's T_c
+    and the value is the better engine's share.  The calls use their default
+    SM budgets: a partitioned mode's split is not applied here."""
     name, mode, split, prio = next(m for m in modes if m[0] == best)
-    engine = c3.C3_ENGINE_CE if mode in (2, 3) else c3.C3_ENGINE_SM
     hA = torch.from_numpy(A_h.view(np.int16)).pin_memory()
     if w.coll == "alltoall":
         hpay = [torch.from_numpy(payload).pin_memory()]
@@ -973,6 +973,7 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
     bi_p = sum(h.numel() * h.element_size() for h in hpay)
     bo = hC.numel() * 4
     s2 = torch.cuda.Stream(dev, priority=-1 if prio else 0)  # -1: a higher priority than the default 0
+    engines = {"sm": c3.C3_ENGINE_SM, "memcpy": c3.C3_ENGINE_CE}
 
     def gemm_chain(s):
         with torch.cuda.stream(s):
@@ -980,7 +981,7 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
             c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, s)
             hC.copy_(dC, non_blocking=True)
 
-    def coll_chain(s):
+    def coll_chain(s, engine):
         if w.coll == "allgather":
             c3.c3_allgather(hpay, out, w.unit_bytes, w.nranks, engine=engine, stream=s)
         elif w.coll == "alltoall":
@@ -1000,34 +1001,50 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e-3
 
-    def conc(e0):
+    def conc(e0, engine):
         s2.wait_event(e0)
         if prio:
-            coll_chain(s2)
+            coll_chain(s2, engine)
             gemm_chain(stream)
         else:
             gemm_chain(stream)
-            coll_chain(s2)
+            coll_chain(s2, engine)
         done = torch.cuda.Event()
         done.record(s2)
         stream.wait_event(done)
 
-    recs = []
+    tgs, tcs, tconcs = [], {e: [] for e in engines}, {e: [] for e in engines}
     for it in range(args.warmup + args.steps):
         tg = timed(lambda e0: gemm_chain(stream))
-        tc = timed(lambda e0: coll_chain(stream))
-        tconc = timed(conc)
+        step = {}
+        for ename, eng in engines.items():
+            step[ename] = (timed(lambda e0: coll_chain(stream, eng)), timed(lambda e0: conc(e0, eng)))
         if it >= args.warmup:
-            recs.append((tg, tc, tconc))
+            tgs.append(tg)
+            for ename, (tc, tconc) in step.items():
+                tcs[ename].append(tc)
+                tconcs[ename].append(tconc)
     c3.c3_status_check(stream)
-    tg = statistics.median(r[0] for r in recs)
-    tc = statistics.median(r[1] for r in recs)
-    tconc = statistics.median(r[2] for r in recs)
-    m = pct_gain(tg, tc, tconc)
-    return {"value": m["pct_ideal_gain"], "unit": UNIT, "h2d_bytes_per_step": 2 * (bi_a + bi_p),
-            "d2h_bytes_per_step": 2 * bo, "mode": best, "t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc,
-            "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"],
-            "engine": "memcpy" if engine == c3.C3_ENGINE_CE else "sm",
+    tg = statistics.median(tgs)
+    tc_med = {e: statistics.median(v) for e, v in tcs.items()}
+    tc_strict = min(tc_med.values())
+    per_engine = {}
+    for e in engines:
+        tconc = statistics.median(tconcs[e])
+        m = pct_gain(tg, tc_strict, tconc)
+        per_engine[e] = {"pct_ideal_gain": m["pct_ideal_gain"], "t_comm_us": 1e6 * tc_med[e],
+                         "t_conc_us": 1e6 * tconc, "s_real": m["s_real"],
+                         "pct_ideal_gain_own_engine": pct_gain(tg, tc_med[e], tconc)["pct_ideal_gain"]}
+    best_engine = max(per_engine, key=lambda e: per_engine[e]["pct_ideal_gain"])
+    pe = per_engine[best_engine]
+    return {"value": pe["pct_ideal_gain"], "unit": UNIT,
+            # per step: A for the GEMM chain and for each engine's concurrent run, the payload for
+            # each engine's collective alone and concurrent run; C back after each GEMM chain
+            "h2d_bytes_per_step": 3 * bi_a + 4 * bi_p, "d2h_bytes_per_step": 3 * bo,
+            "mode": best, "engine": best_engine, "t_gemm_us": 1e6 * tg, "t_comm_us": pe["t_comm_us"],
+            "t_comm_strict_us": 1e6 * tc_strict, "t_conc_us": pe["t_conc_us"],
+            "s_ideal": pct_gain(tg, tc_strict, 1.0)["s_ideal"], "s_real": pe["s_real"],
+            "engines": per_engine,
             "collective_sources": ("copied to HBM first (the reduction needs device inputs)" if w.coll == "allreduce"
                                    else "pinned host memory, read by the collective itself")}
 
