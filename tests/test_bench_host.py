@@ -1,0 +1,89 @@
+"""Host logic of bench.py on the CPU: the post-run validation's restated
+definitions agree with the oracle and reject a planted error, the metric
+arithmetic matches the oracle's closed forms, and the taxonomy, strict T_comm,
+dispersion and workload lookup behave as documented."""
+import math
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import oracle  # noqa: E402
+from concurrent_communication_overlap_gb300 import inputs as I  # noqa: E402
+
+
+@pytest.mark.parametrize("name", ["tiny_ag", "tiny_a2a", "tiny_ar"])
+def test_expected_collective_is_the_oracles(name):
+    w = I.WORKLOADS[name]
+    pay = I.coll_payload(w)
+    got = bench.expected_collective(np, w, pay)
+    if w.coll == "allgather":
+        ref = oracle.allgather(pay)
+    elif w.coll == "alltoall":
+        ref = oracle.alltoall(pay, w.nranks)
+    else:
+        ref = oracle.allreduce(pay)[0].reshape(-1).view(np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_gemm_rows_check_accepts_exact_rows_and_rejects_an_error():
+    w = I.WORKLOADS["tiny_ag"]
+    A, B = I.gemm_operands(w)
+    rows = np.array([0, 1, 255, 511])
+    C, S = oracle.gemm(A[rows], B)
+    ref = bench.gemm_rows_reference(np, A, B, rows)
+    assert bench.gemm_rows_ok(np, A, B, rows, C.astype(np.float32), ref)
+    bad = C.astype(np.float32).copy()
+    bad[2, 7] += 1e-2 * S[2, 7]              # one entry off by 100x the tolerance
+    assert not bench.gemm_rows_ok(np, A, B, rows, bad, ref)
+    nan = C.astype(np.float32).copy()
+    nan[0, 0] = np.nan                        # an unwritten output
+    assert not bench.gemm_rows_ok(np, A, B, rows, nan, ref)
+
+
+@pytest.mark.parametrize("tg,tc,tconc", [(100.0, 42.0, 130.0), (2.0, 2.0, 2.0), (50.0, 80.0, 90.0),
+                                         (7.0, 3.0, 10.0)])
+def test_metric_arithmetic_matches_the_oracle(tg, tc, tconc):
+    m = bench.pct_gain(tg, tc, tconc)
+    o = oracle.c3_metrics(tg, tc, tconc)
+    assert math.isclose(m["s_ideal"], o["s_ideal"], rel_tol=1e-12)
+    assert math.isclose(m["s_real"], o["s_real"], rel_tol=1e-12)
+    assert math.isclose(m["pct_ideal_gain"], 100.0 * o["pct_ideal_gain"], rel_tol=1e-12, abs_tol=1e-12)
+    assert math.isclose(m["pct_ideal_ratio"], 100.0 * o["pct_ideal_ratio"], rel_tol=1e-12)
+    assert bench.c3_class(tg, tc) == o["class"]
+
+
+def test_taxonomy_thresholds():
+    assert bench.c3_class(115.0, 100.0) == "G-long"
+    assert bench.c3_class(114.9, 100.0) == "GC-equal"
+    assert bench.c3_class(100.0, 115.0) == "C-long"
+    assert bench.c3_class(100.0, 100.0) == "GC-equal"
+
+
+def test_strict_comm_time_is_the_faster_engines_median():
+    modes = [("baseline", 1, 0, 0), ("ce", 2, 0, 0), ("ce_rp_8", 2, 8, 0)]
+    per_mode = {"baseline": [{"t_comm_iso": t} for t in (5.0, 6.0, 7.0)],
+                "ce": [{"t_comm_iso": t} for t in (4.0, 9.0)],
+                "ce_rp_8": [{"t_comm_iso": t} for t in (10.0,)]}
+    # SM engine median 6.0; memcpy engine median of (4, 9, 10) = 9.0
+    assert bench.strict_comm_time(per_mode, modes) == 6.0
+
+
+def test_spread_ignores_missing_values():
+    s = bench.spread([3.0, None, float("nan"), 1.0, 2.0])
+    assert s == {"median": 2.0, "min": 1.0, "max": 3.0, "stdev": pytest.approx(math.sqrt(2.0 / 3.0)), "n": 3}
+    assert bench.spread([None]) is None
+
+
+def test_workload_lookup():
+    assert bench.find_workload(I, "mem_ag") is I.WORKLOADS["mem_ag"]
+    w = bench.find_workload(I, "sweep_alltoall_4194304k")
+    assert (w.M, w.N, w.K, w.coll, w.coll_bytes) == (8192, 8192, 8192, "alltoall", 4 << 30)
+    with pytest.raises(SystemExit):
+        bench.find_workload(I, "no_such_workload")
