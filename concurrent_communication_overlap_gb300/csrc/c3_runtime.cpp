@@ -658,7 +658,7 @@ int c3_allgather(const void* const* shards, void* out, size_t shard_bytes, int n
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
     if ((rc = locate_plan(*ds, &t))) return rc;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCeGraph, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int engine, int sm_budget,
@@ -672,7 +672,7 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
     if ((rc = locate_plan(*ds, &t))) return rc;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCeGraph, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
 int c3_inject_fault(int site) {
@@ -711,7 +711,7 @@ int c3_allreduce(const float* const* inputs, float* out, size_t count, int nrank
     DeviceState* ds = device_state();
     if (!ds) return C3_ECUDA;
     if ((rc = locate_plan(*ds, &t))) return rc;
-    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCePerSegment, sm_budget, false, static_cast<cudaStream_t>(s),
+    return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCeGraph, sm_budget, false, static_cast<cudaStream_t>(s),
                        nullptr);
 }
 

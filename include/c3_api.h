@@ -186,7 +186,8 @@ int c3_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_budget, int *bn, int *m
  *   nranks  1..64
  *   engine  C3_ENGINE_SM: an SM copy kernel on `sm_budget` SMs (0 = default
  *           budget; host shards are read with plain loads over the CPU-GPU
- *           link); C3_ENGINE_CE: one cudaMemcpyAsync per shard, sm_budget
+ *           link); C3_ENGINE_CE: the driver memcpy path, one transfer per
+ *           shard replayed from a cached CUDA graph (C3_CE_GRAPH), sm_budget
  *           ignored.
  * Bit-exact byte copy.  Asynchronous on `s`.
  */
@@ -202,7 +203,8 @@ int c3_allgather(const void *const *shards, void *out, size_t shard_bytes, int n
  *            memory, in is device or page-locked host memory (as for shards)
  *   block_bytes multiple of 16 (else C3_EALIGN); 0 launches nothing
  *   nranks  1..8 (the SM kernel's segment table holds 64 blocks)
- *   engine  as for c3_allgather (CE: one cudaMemcpyAsync per block)
+ *   engine  as for c3_allgather (CE: one strided 2-D transfer per source rank,
+ *           replayed from a cached CUDA graph)
  * Bit-exact.  Asynchronous on `s`.
  */
 int c3_alltoall(const void *in, void *out, size_t block_bytes, int nranks, int engine,
