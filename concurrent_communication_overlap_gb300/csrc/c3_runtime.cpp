@@ -505,16 +505,28 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // free SM start when the collective's SMs free up
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
+        bool comm_launched = false;
         auto go_gemm = [&] { return gemm_enqueue(gl, sg, ds.status, &gctas); };
-        auto go_comm = [&] { return launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas); };
+        auto go_comm = [&] {
+            int r = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas);
+            comm_launched = (r == C3_OK);
+            return r;
+        };
+        // A failure after the collective went out still orders the caller's
+        // stream after it, so that the caller may reuse its buffers once its
+        // own stream has drained.
+        auto fail = [&](int code) {
+            if (comm_launched && cudaEventRecord(ev_c, sc) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c, 0);
+            return code;
+        };
         if (priority || reclaim) {
             if ((rc = go_comm())) return rc;
-            if ((rc = go_gemm())) return rc;
+            if ((rc = go_gemm())) return fail(rc);
         } else {
             if ((rc = go_gemm())) return rc;
             if ((rc = go_comm())) return rc;
         }
-        if ((e = cudaEventRecord(ev_g, sg)) != cudaSuccess) return set_cuda_error(e, "event record");
+        if ((e = cudaEventRecord(ev_g, sg)) != cudaSuccess) return fail(set_cuda_error(e, "event record"));
         if ((e = cudaEventRecord(ev_c, sc)) != cudaSuccess) return set_cuda_error(e, "event record");
         if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
     }

@@ -87,8 +87,8 @@ def test_injected_collective_failure_is_reported_and_recovers(engine, site):
     assert c3.c3_status_check() == c3.C3_OK and ok()
 
 
-@pytest.mark.parametrize("mode,site", [(1, 2), (1, 1), (2, 3), (4, 2)])
-def test_injected_failure_inside_a_concurrent_run(mode, site):
+@pytest.mark.parametrize("mode,site,priority", [(1, 2, 0), (1, 1, 0), (2, 3, 0), (4, 2, 0), (1, 1, 1), (4, 1, 0)])
+def test_injected_failure_inside_a_concurrent_run(mode, site, priority):
     # one half of the pair fails after (or before) the other was launched: the
     # run reports C3_ECUDA, and the next run of the same problem is exact
     import ctypes
@@ -99,8 +99,13 @@ def test_injected_failure_inside_a_concurrent_run(mode, site):
     split = 16 if mode == 4 else 0
     c3.c3_inject_fault(site)
     t = c3.C3Timing()
-    assert c3.lib().c3_run(ctypes.byref(p.rec), mode, split, 0, ctypes.byref(t)) == c3.C3_ECUDA
+    assert c3.lib().c3_run(ctypes.byref(p.rec), mode, split, priority, ctypes.byref(t)) == c3.C3_ECUDA
     assert "injected" in c3.c3_last_error()
+    if site == c3.C3_FAULT_GEMM_LAUNCH and (priority or mode == 4):
+        # the collective went out before the GEMM's launch failed: it completes,
+        # ordered before the caller's own stream
+        torch.cuda.current_stream().synchronize()
+        assert coll_ok() and torch.isnan(dC).all()
     torch.cuda.synchronize()
     dC.fill_(float("nan"))
     out.zero_()
