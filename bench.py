@@ -11,11 +11,13 @@ weights, fp32 out) with an all-gather of an 8192x8192 bf16 weight from 8
 virtual ranks (8 x 16 MiB).
 
 value = realized share of the ideal C3 gain, (S_real - 1) / (S_ideal - 1), of
-the best mode, from the medians over the timed steps (S_ideal = (T_g + T_c) /
+the best mode, from the means over the timed steps (S_ideal = (T_g + T_c) /
 max(T_g, T_c) with isolated times; S_real = (T_g + T_c) / T_concurrent).  T_c
 is the strict one: the fastest isolated collective of any engine measured, so
 a mode cannot look better by having a slow collective of its own; the share
-against the mode's own engine is reported beside it.
+against the mode's own engine is reported beside it.  Means, as the pages
+average their runs: CUDA event times on GB300 come in steps of about 2 us, so a
+median snaps to a step while the mean over many steps resolves below one.
 
 ``--impl reference`` times the CPU oracle on the same workload (a bounded
 sample of it) through the same C3 procedure; it is the reference arm.
@@ -181,21 +183,28 @@ def c3_class(tg, tc):
     return "GC-equal"
 
 
+def step_mean(xs):
+    """The per-step statistic every C3 time is summarised by: the mean over
+    the timed steps (the pages average their runs; the event clock's ~2 us
+    steps bias a median to a step, not a mean over many steps)."""
+    return statistics.fmean(xs)
+
+
 def strict_comm_time(per_mode, modes):
-    """The fastest isolated collective over the engines measured (median per
+    """The fastest isolated collective over the engines measured (mean per
     engine): the strict T_comm for every mode's ideal."""
     by_engine = {}
     for name, mode, split, prio in modes:
         eng = "ce" if mode in (2, 3) else "sm"
         by_engine.setdefault(eng, []).extend(r["t_comm_iso"] for r in per_mode[name])
-    return min(statistics.median(v) for v in by_engine.values() if v)
+    return min(step_mean(v) for v in by_engine.values() if v)
 
 
 def spread(xs):
     xs = [x for x in xs if x is not None and not (isinstance(x, float) and math.isnan(x))]
     if not xs:
         return None
-    return {"median": statistics.median(xs), "min": min(xs), "max": max(xs),
+    return {"mean": statistics.fmean(xs), "median": statistics.median(xs), "min": min(xs), "max": max(xs),
             "stdev": statistics.pstdev(xs) if len(xs) > 1 else 0.0, "n": len(xs)}
 
 
@@ -425,9 +434,9 @@ def cpu_c3(w, steps, warmup, rows=None, target_s=1.0):
 
 
 def summarize_cpu(recs):
-    tg = statistics.median(r[0] for r in recs)
-    tc = statistics.median(r[1] for r in recs)
-    tconc = statistics.median(r[2] for r in recs)
+    tg = step_mean([r[0] for r in recs])
+    tc = step_mean([r[1] for r in recs])
+    tconc = step_mean([r[2] for r in recs])
     return pct_gain(tg, tc, tconc), (tg, tc, tconc)
 
 
@@ -517,9 +526,9 @@ def run_sweep(args, c3, torch, np, I, dev, info):
         res = {}
         tc_strict = strict_comm_time(per, modes)
         for name, recs in per.items():
-            tg = statistics.median(r["t_gemm_iso"] for r in recs)
-            tc = statistics.median(r["t_comm_iso"] for r in recs)
-            tconc = statistics.median(r["t_conc"] for r in recs)
+            tg = step_mean([r["t_gemm_iso"] for r in recs])
+            tc = step_mean([r["t_comm_iso"] for r in recs])
+            tconc = step_mean([r["t_conc"] for r in recs])
             m = pct_gain(tg, tc_strict, tconc)
             m_own = pct_gain(tg, tc, tconc)
             res[name] = {"t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc, "t_comm_strict_us": 1e6 * tc_strict,
@@ -757,7 +766,7 @@ def main(argv=None):
         per_mode_ok[name] = outputs_ok()
     torch.cuda.synchronize(dev)
 
-    # ---- statistics per mode (medians over the timed steps)
+    # ---- statistics per mode (means over the timed steps)
     peaks = load_peaks()
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     gemm_hbm_bound = w.gemm_flops / w.gemm_bytes < ridge
@@ -774,19 +783,19 @@ def main(argv=None):
     all_tg = [r["t_gemm_iso"] for recs in per_mode.values() for r in recs]
     tc_strict = strict_comm_time(per_mode, modes)
     for name, recs in per_mode.items():
-        tg = statistics.median(r["t_gemm_iso"] for r in recs)
-        tc = statistics.median(r["t_comm_iso"] for r in recs)
-        tconc = statistics.median(r["t_conc"] for r in recs)
+        tg = step_mean([r["t_gemm_iso"] for r in recs])
+        tc = step_mean([r["t_comm_iso"] for r in recs])
+        tconc = step_mean([r["t_conc"] for r in recs])
         m = pct_gain(tg, tc_strict, tconc)
         m_own = pct_gain(tg, tc, tconc)
-        tgd = statistics.median(r["t_gemm_dev"] for r in recs)
+        tgd = step_mean([r["t_gemm_dev"] for r in recs])
         # the SM collective's own kernel window when it is all on SMs; fork-to-done
         # events when the memcpy path carries all or part of it
         tcd = [r["t_comm_dev"] if (r["comm_ctas"] and r["mode"] in (0, 1)) else r["t_comm_ev"] for r in recs]
         stats[name] = {
             "t_gemm_iso_us": 1e6 * tg, "t_comm_iso_us": 1e6 * tc, "t_comm_iso_strict_us": 1e6 * tc_strict,
             "t_conc_us": 1e6 * tconc,
-            "t_serial_meas_us": 1e6 * statistics.median(r["t_serial_meas"] for r in recs),
+            "t_serial_meas_us": 1e6 * step_mean([r["t_serial_meas"] for r in recs]),
             "s_ideal": m["s_ideal"], "s_real": m["s_real"],
             "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
@@ -794,15 +803,15 @@ def main(argv=None):
             "spread_us": {k: spread([1e6 * r[k] for r in recs]) for k in ("t_gemm_iso", "t_comm_iso", "t_conc")},
             "class": c3_class(tg, tc_strict), "class_own_engine": c3_class(tg, tc),
             "gemm_tflops_overlap": w.gemm_flops / tgd / 1e12 if tgd > 0 else None,
-            "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / statistics.median(tcd) / 1e9
-                                 if statistics.median(tcd) > 0 else None),
+            "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / step_mean(tcd) / 1e9
+                                 if step_mean(tcd) > 0 else None),
             "gemm_slowdown": tgd / tg if tg > 0 else None,
             # roofline fractions: the GEMM against HBM or the tensor peak (whichever bounds it),
             # isolated (event time) and under overlap (its device window); the SM copy against HBM
             "gemm_roofline_frac_iso": gemm_frac(tg),
             "gemm_roofline_frac_overlap": gemm_frac(tgd),
-            "copy_roofline_frac_overlap": (w.coll_traffic_bytes / statistics.median(tcd) / 1e9 / peaks["hbm_gbs"]
-                                           if statistics.median(tcd) > 0 and not host_src else None),
+            "copy_roofline_frac_overlap": (w.coll_traffic_bytes / step_mean(tcd) / 1e9 / peaks["hbm_gbs"]
+                                           if step_mean(tcd) > 0 and not host_src else None),
             "gemm_ctas": recs[0]["gemm_ctas"], "comm_ctas": recs[0]["comm_ctas"],
             "smid_overlap_max": max(r["smid_overlap"] for r in recs),
         }
@@ -825,7 +834,7 @@ def main(argv=None):
     roof["kernel"] = "gemm_bf16_kernel (tcgen05)"
     roof["algorithmic_per_launch"] = w.gemm_bytes if roof["bound"] == "hbm" else w.gemm_flops
     roof["peak_source"] = f"{peaks['source']} (burst)"
-    tc_sm = statistics.median(r["t_comm_iso"] for r in per_mode["baseline"]) if "baseline" in per_mode else None
+    tc_sm = step_mean([r["t_comm_iso"] for r in per_mode["baseline"]]) if "baseline" in per_mode else None
     copy_roof = None
     if tc_sm and host_src:
         # the sources cross the CPU-GPU link: the link, not HBM, bounds the copy,
@@ -1025,12 +1034,12 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
                 tcs[ename].append(tc)
                 tconcs[ename].append(tconc)
     c3.c3_status_check(stream)
-    tg = statistics.median(tgs)
-    tc_med = {e: statistics.median(v) for e, v in tcs.items()}
+    tg = step_mean(tgs)
+    tc_med = {e: step_mean(v) for e, v in tcs.items()}
     tc_strict = min(tc_med.values())
     per_engine = {}
     for e in engines:
-        tconc = statistics.median(tconcs[e])
+        tconc = step_mean(tconcs[e])
         m = pct_gain(tg, tc_strict, tconc)
         per_engine[e] = {"pct_ideal_gain": m["pct_ideal_gain"], "t_comm_us": 1e6 * tc_med[e],
                          "t_conc_us": 1e6 * tconc, "s_real": m["s_real"],

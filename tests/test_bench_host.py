@@ -66,18 +66,28 @@ def test_taxonomy_thresholds():
     assert bench.c3_class(100.0, 100.0) == "GC-equal"
 
 
-def test_strict_comm_time_is_the_faster_engines_median():
+def test_strict_comm_time_is_the_faster_engines_mean():
     modes = [("baseline", 1, 0, 0), ("ce", 2, 0, 0), ("ce_rp_8", 2, 8, 0)]
-    per_mode = {"baseline": [{"t_comm_iso": t} for t in (5.0, 6.0, 7.0)],
-                "ce": [{"t_comm_iso": t} for t in (4.0, 9.0)],
-                "ce_rp_8": [{"t_comm_iso": t} for t in (10.0,)]}
-    # SM engine median 6.0; memcpy engine median of (4, 9, 10) = 9.0
-    assert bench.strict_comm_time(per_mode, modes) == 6.0
+    per_mode = {"baseline": [{"t_comm_iso": t} for t in (5.0, 6.0, 10.0)],
+                "ce": [{"t_comm_iso": t} for t in (6.5, 6.5)],
+                "ce_rp_8": [{"t_comm_iso": t} for t in (6.5,)]}
+    # SM engine: mean 7.0 (median 6.0); memcpy engine: mean 6.5 over both memcpy modes
+    assert bench.strict_comm_time(per_mode, modes) == 6.5
+
+
+def test_step_mean_resolves_below_the_clock_step():
+    # times that snap to a 2.048 us clock: the mean recovers the true centre,
+    # a median can only return a clock step
+    tick = 2.048
+    samples = [tick * 60] * 3 + [tick * 61] * 2
+    assert bench.step_mean(samples) == pytest.approx(tick * 60.4)
+    assert bench.step_mean(samples) not in samples
 
 
 def test_spread_ignores_missing_values():
     s = bench.spread([3.0, None, float("nan"), 1.0, 2.0])
-    assert s == {"median": 2.0, "min": 1.0, "max": 3.0, "stdev": pytest.approx(math.sqrt(2.0 / 3.0)), "n": 3}
+    assert s == {"mean": 2.0, "median": 2.0, "min": 1.0, "max": 3.0, "stdev": pytest.approx(math.sqrt(2.0 / 3.0)),
+                 "n": 3}
     assert bench.spread([None]) is None
 
 
