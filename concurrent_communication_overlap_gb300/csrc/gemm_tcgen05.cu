@@ -59,12 +59,17 @@ struct GemmCfg {
                                           : kUsedCols <= 256 ? 256 : 512;
     // Epilogue staging: two 4 KiB blocks (32 rows x 128 B) per epilogue warp.
     // Its own region when the ring leaves room for it; otherwise the CTA's
-    // last tile borrows the (then idle) first ring stage, and earlier tiles
-    // store directly.
+    // last tile borrows the (then idle) ring, and earlier tiles store
+    // directly.
     static constexpr int kStagingBytes = 4 * 2 * 4096;
     static constexpr bool kOwnStaging =
         kSmemLimit - 1024 - 512 - kStages * (int)kStageBytes >= kStagingBytes;
-    static_assert(kOwnStaging || (int)kStageBytes >= kStagingBytes, "no room to stage the epilogue");
+    // A last tile staged in the idle ring gives each epilogue warp a quarter of
+    // it: room for every 4 KiB block of its lane quarter, so no block is reused
+    // and no store has to be waited for before the next block is written.
+    static constexpr int kRingBlocksPerWarp = kStages * (int)kStageBytes / (4 * 4096);
+    static constexpr int kBlocksPerWarp = MSUB * BN / 32;
+    static_assert(kOwnStaging || kRingBlocksPerWarp >= kBlocksPerWarp, "no room to stage the epilogue");
     // ring, [staging], then barriers / TMEM slot / abort flag (512 B), plus 1 KiB for alignment
     static constexpr int kSmem = kStages * kStageBytes + (kOwnStaging ? kStagingBytes : 0) + 1024 + 512;
     static_assert(kStages >= 2, "tile too large for the shared-memory ring");
@@ -306,10 +311,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_REMPTY + slot));
             if (t >= total_tiles) break;
-            // Where this tile's output is staged: the own region, or the first
-            // ring stage when this is the CTA's last tile (the producer then
-            // loads nothing more, and every stage has been consumed once the
-            // accumulator is ready).  The next tile-ring entry is already
+            // Where this tile's output is staged: the own region, or the ring
+            // when this is the CTA's last tile (the producer then loads nothing
+            // more, and every stage has been consumed once the accumulator is
+            // ready).  The next tile-ring entry is already
             // published by then: the producer writes it as soon as it has
             // issued this tile's last load.
             bool staged = false;
@@ -342,13 +347,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int mb, nb;
             tile_coords(t, num_m, num_n, mb, nb);
             if (staged) {
-                // Two 4 KiB blocks per warp, alternating; a block is rewritten
-                // only after the TMA store issued from it two blocks ago has
-                // read it.  Row `lane` of a block holds 32 fp32 in eight 16-byte
-                // chunks, chunk j at position j ^ (lane & 7): the 128-byte
-                // swizzle the store's tensor map undoes, and no bank conflicts
-                // beyond the four wavefronts 512 bytes need.
-                const uint32_t wstg = stg + (uint32_t)q * 8192u;
+                // Own region: two 4 KiB blocks per warp, alternating; a block is
+                // rewritten only after the TMA store issued from it two blocks
+                // ago has read it.  Idle ring (last tile): one block per 32x32
+                // piece, never reused.  Row `lane` of a block holds 32 fp32 in
+                // eight 16-byte chunks, chunk j at position j ^ (lane & 7): the
+                // 128-byte swizzle the store's tensor map undoes, and no bank
+                // conflicts beyond the four wavefronts 512 bytes need.
+                const uint32_t wstg =
+                    stg + (uint32_t)q * (Cfg::kOwnStaging ? 8192u : (uint32_t)Cfg::kRingBlocksPerWarp * 4096u);
                 int issued = 0;
 #pragma unroll 1
                 for (int sub = 0; sub < MSUB; ++sub) {
@@ -367,8 +374,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         }
                         const int col0 = nb * BN + c * 32;
                         if (row0 >= M || col0 >= N) continue;  // wholly outside C (uniform per warp)
-                        const uint32_t blk = wstg + (uint32_t)(issued & 1) * 4096u;
-                        if (issued >= 2) {
+                        const uint32_t blk = wstg + (uint32_t)(Cfg::kOwnStaging ? (issued & 1) : issued) * 4096u;
+                        if (Cfg::kOwnStaging && issued >= 2) {
                             if (lane == 0) bulk_wait_read<1>();
                             __syncwarp();
                         }
