@@ -314,7 +314,10 @@ typedef struct {
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error
- * (nothing launched) or the device status of the run.
+ * (nothing launched) or the device status of the run.  If a launch fails after
+ * the collective went out (prioritised and reclaim modes launch it first), the
+ * call returns C3_ECUDA with p->stream still ordered after the collective, so
+ * the caller may reuse the buffers once that stream has drained.
  */
 int c3_run(const c3_problem *p, int mode, int sm_split, int priority, c3_timing *out);
 
