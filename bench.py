@@ -110,7 +110,7 @@ def parse_args(argv=None):
 
 def pct_gain(tg, tc, tconc):
     """Share of the ideal gain and the plain ratio (host-side restatement of
-    the library's c3_timing fields, used for medians of times)."""
+    the library's c3_timing fields, applied to the per-step means)."""
     serial = tg + tc
     longest = max(tg, tc)
     s_ideal = serial / longest
@@ -198,6 +198,30 @@ def strict_comm_time(per_mode, modes):
         eng = "ce" if mode in (2, 3) else "sm"
         by_engine.setdefault(eng, []).extend(r["t_comm_iso"] for r in per_mode[name])
     return min(step_mean(v) for v in by_engine.values() if v)
+
+
+def share_ci95(recs, tc_strict, n_boot=400, seed=0):
+    """95% bootstrap interval of a mode's share of the ideal gain (percent):
+    the timed steps are resampled with replacement and T_g and T_conc
+    re-averaged, with the strict T_c held at its full-sample mean.  Shows how
+    far step-to-step noise can move the share; it is wide wherever S_ideal - 1
+    is small.  None with fewer than 3 steps."""
+    import numpy as np
+    if len(recs) < 3 or not tc_strict or tc_strict <= 0:
+        return None
+    tg = np.array([r["t_gemm_iso"] for r in recs], dtype=np.float64)
+    tconc = np.array([r["t_conc"] for r in recs], dtype=np.float64)
+    idx = np.random.default_rng(seed).integers(0, len(recs), size=(n_boot, len(recs)))
+    g, c = tg[idx].mean(axis=1), tconc[idx].mean(axis=1)
+    serial = g + tc_strict
+    s_ideal = serial / np.maximum(g, tc_strict)
+    s_real = serial / c
+    ok = s_ideal > 1.0
+    if not ok.any():
+        return None
+    share = 100.0 * (s_real[ok] - 1.0) / (s_ideal[ok] - 1.0)
+    lo, hi = np.percentile(share, [2.5, 97.5])
+    return [float(lo), float(hi)]
 
 
 def spread(xs):
@@ -533,7 +557,8 @@ def run_sweep(args, c3, torch, np, I, dev, info):
             m_own = pct_gain(tg, tc, tconc)
             res[name] = {"t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc, "t_comm_strict_us": 1e6 * tc_strict,
                          "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"],
-                         "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
+                         "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_gain_ci95": share_ci95(recs, tc_strict),
+                         "pct_ideal_ratio": m["pct_ideal_ratio"],
                          "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "class": c3_class(tg, tc_strict)}
         best = max(res, key=lambda k: res[k]["pct_ideal_gain"] if res[k]["s_ideal"] > 1.0 else -1e9)
         print(json.dumps({"sweep": args.sweep, "workload": w.name, "coll_bytes": w.coll_bytes, "steps": args.steps,
@@ -797,7 +822,8 @@ def main(argv=None):
             "t_conc_us": 1e6 * tconc,
             "t_serial_meas_us": 1e6 * step_mean([r["t_serial_meas"] for r in recs]),
             "s_ideal": m["s_ideal"], "s_real": m["s_real"],
-            "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_ratio": m["pct_ideal_ratio"],
+            "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_gain_ci95": share_ci95(recs, tc_strict),
+            "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
             "pct_ideal_gain_own_engine_per_step": spread([100.0 * r["pct_ideal_gain"] for r in recs]),
             "spread_us": {k: spread([1e6 * r[k] for r in recs]) for k in ("t_gemm_iso", "t_comm_iso", "t_conc")},
@@ -863,6 +889,8 @@ def main(argv=None):
                                 else "device memory (8 emulated ranks in one HBM)"),
                    "modes": [m[0] for m in modes]},
         "best_mode": best,
+        # rank 0's replica: bootstrap over its timed steps
+        "value_ci95": stats[best]["pct_ideal_gain_ci95"],
         "gemm_tflops_overlap": stats[best]["gemm_tflops_overlap"],
         "copy_gbs_overlap": stats[best]["copy_gbs_overlap"],
         "roofline": roof, "roofline_copy": copy_roof,

@@ -97,3 +97,32 @@ def test_workload_lookup():
     assert (w.M, w.N, w.K, w.coll, w.coll_bytes) == (8192, 8192, 8192, "alltoall", 4 << 30)
     with pytest.raises(SystemExit):
         bench.find_workload(I, "no_such_workload")
+
+
+def _recs(tg, tconc):
+    return [{"t_gemm_iso": a, "t_conc": b} for a, b in zip(tg, tconc)]
+
+
+def test_share_ci_of_constant_steps_is_the_point_estimate():
+    recs = _recs([100.0] * 10, [120.0] * 10)
+    point = bench.pct_gain(100.0, 40.0, 120.0)["pct_ideal_gain"]
+    lo, hi = bench.share_ci95(recs, 40.0)
+    assert lo == pytest.approx(point) and hi == pytest.approx(point)
+    assert bench.share_ci95(recs[:2], 40.0) is None
+
+
+def test_share_ci_covers_the_estimate_and_narrows_with_more_steps():
+    rng = np.random.default_rng(7)
+
+    def draw(n):
+        return _recs(100.0 + rng.normal(0, 1.0, n), 125.0 + rng.normal(0, 1.0, n))
+    few, many = draw(20), draw(320)
+    for recs in (few, many):
+        tg = bench.step_mean([r["t_gemm_iso"] for r in recs])
+        tconc = bench.step_mean([r["t_conc"] for r in recs])
+        point = bench.pct_gain(tg, 42.0, tconc)["pct_ideal_gain"]
+        lo, hi = bench.share_ci95(recs, 42.0)
+        assert lo < point < hi
+    w_few = bench.share_ci95(few, 42.0)
+    w_many = bench.share_ci95(many, 42.0)
+    assert (w_many[1] - w_many[0]) < 0.5 * (w_few[1] - w_few[0])      # ~1/sqrt(16) in theory
