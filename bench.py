@@ -994,12 +994,13 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
     pinned host buffers (c3_allgather / c3_alltoall accept page-locked host
     sources; the all-reduce, whose reduction needs device inputs, copies them
     in first).  T_g = the GEMM chain alone, T_c = the collective alone, T_conc
-    = both chains at once on two streams (the collective's on a high-priority
-    stream if the best device mode is prioritised).  Both engines are
-    measured; as on the device side, the ideal uses the faster engine's T_c
-    and the value is the better engine's share.  The calls use their default
-    SM budgets: a partitioned mode's split is not applied here."""
-    name, mode, split, prio = next(m for m in modes if m[0] == best)
+    = both chains at once on two streams.  Four concurrent variants run every
+    step: each engine, with the GEMM chain launched first and the collective
+    on a default-priority stream (baseline) or the collective launched first
+    on a high-priority stream (prioritised).  As on the device side, the ideal
+    uses the faster engine's T_c and the value is the best variant's share.
+    The calls use their default SM budgets: a partitioned mode's split is not
+    applied here."""
     hA = torch.from_numpy(A_h.view(np.int16)).pin_memory()
     if w.coll == "alltoall":
         hpay = [torch.from_numpy(payload).pin_memory()]
@@ -1009,8 +1010,10 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
     bi_a = hA.numel() * 2
     bi_p = sum(h.numel() * h.element_size() for h in hpay)
     bo = hC.numel() * 4
-    s2 = torch.cuda.Stream(dev, priority=-1 if prio else 0)  # -1: a higher priority than the default 0
+    side = {0: torch.cuda.Stream(dev, priority=0),
+            1: torch.cuda.Stream(dev, priority=-1)}  # -1: a higher priority than the default 0
     engines = {"sm": c3.C3_ENGINE_SM, "memcpy": c3.C3_ENGINE_CE}
+    variants = [(f"{e}{'_prioritised' if p else ''}", e, p) for e in engines for p in (0, 1)]
 
     def gemm_chain(s):
         with torch.cuda.stream(s):
@@ -1038,7 +1041,8 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) * 1e-3
 
-    def conc(e0, engine):
+    def conc(e0, engine, prio):
+        s2 = side[prio]
         s2.wait_event(e0)
         if prio:
             coll_chain(s2, engine)
@@ -1050,38 +1054,40 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out,
         done.record(s2)
         stream.wait_event(done)
 
-    tgs, tcs, tconcs = [], {e: [] for e in engines}, {e: [] for e in engines}
+    tgs, tcs, tconcs = [], {e: [] for e in engines}, {v[0]: [] for v in variants}
     for it in range(args.warmup + args.steps):
         tg = timed(lambda e0: gemm_chain(stream))
-        step = {}
-        for ename, eng in engines.items():
-            step[ename] = (timed(lambda e0: coll_chain(stream, eng)), timed(lambda e0: conc(e0, eng)))
+        alone = {e: timed(lambda e0: coll_chain(stream, engines[e])) for e in engines}
+        together = {v: timed(lambda e0: conc(e0, engines[e], p)) for v, e, p in variants}
         if it >= args.warmup:
             tgs.append(tg)
-            for ename, (tc, tconc) in step.items():
-                tcs[ename].append(tc)
-                tconcs[ename].append(tconc)
+            for e, t in alone.items():
+                tcs[e].append(t)
+            for v, t in together.items():
+                tconcs[v].append(t)
     c3.c3_status_check(stream)
     tg = step_mean(tgs)
-    tc_med = {e: step_mean(v) for e, v in tcs.items()}
-    tc_strict = min(tc_med.values())
-    per_engine = {}
-    for e in engines:
-        tconc = step_mean(tconcs[e])
+    tc_mean = {e: step_mean(v) for e, v in tcs.items()}
+    tc_strict = min(tc_mean.values())
+    per_variant = {}
+    for v, e, p in variants:
+        tconc = step_mean(tconcs[v])
         m = pct_gain(tg, tc_strict, tconc)
-        per_engine[e] = {"pct_ideal_gain": m["pct_ideal_gain"], "t_comm_us": 1e6 * tc_med[e],
-                         "t_conc_us": 1e6 * tconc, "s_real": m["s_real"],
-                         "pct_ideal_gain_own_engine": pct_gain(tg, tc_med[e], tconc)["pct_ideal_gain"]}
-    best_engine = max(per_engine, key=lambda e: per_engine[e]["pct_ideal_gain"])
-    pe = per_engine[best_engine]
+        per_variant[v] = {"pct_ideal_gain": m["pct_ideal_gain"], "t_comm_us": 1e6 * tc_mean[e],
+                          "t_conc_us": 1e6 * tconc, "s_real": m["s_real"],
+                          "pct_ideal_gain_own_engine": pct_gain(tg, tc_mean[e], tconc)["pct_ideal_gain"]}
+    best_v = max(per_variant, key=lambda v: per_variant[v]["pct_ideal_gain"])
+    _, best_e, best_p = next(x for x in variants if x[0] == best_v)
+    pe = per_variant[best_v]
     return {"value": pe["pct_ideal_gain"], "unit": UNIT,
-            # per step: A for the GEMM chain and for each engine's concurrent run, the payload for
-            # each engine's collective alone and concurrent run; C back after each GEMM chain
-            "h2d_bytes_per_step": 3 * bi_a + 4 * bi_p, "d2h_bytes_per_step": 3 * bo,
-            "mode": best, "engine": best_engine, "t_gemm_us": 1e6 * tg, "t_comm_us": pe["t_comm_us"],
-            "t_comm_strict_us": 1e6 * tc_strict, "t_conc_us": pe["t_conc_us"],
+            # per step: A for the GEMM chain alone and in each of the 4 concurrent variants; the
+            # payload for each engine's collective alone and in each concurrent variant; C back
+            # after each GEMM chain
+            "h2d_bytes_per_step": 5 * bi_a + 6 * bi_p, "d2h_bytes_per_step": 5 * bo,
+            "mode": "prioritised" if best_p else "baseline", "engine": best_e, "t_gemm_us": 1e6 * tg,
+            "t_comm_us": pe["t_comm_us"], "t_comm_strict_us": 1e6 * tc_strict, "t_conc_us": pe["t_conc_us"],
             "s_ideal": pct_gain(tg, tc_strict, 1.0)["s_ideal"], "s_real": pe["s_real"],
-            "engines": per_engine,
+            "variants": per_variant,
             "collective_sources": ("copied to HBM first (the reduction needs device inputs)" if w.coll == "allreduce"
                                    else "pinned host memory, read by the collective itself")}
 
