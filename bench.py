@@ -908,8 +908,7 @@ def main(argv=None):
     if not args.no_aux:
         line["aux"] = aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info)
     if not args.no_e2e:
-        line["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out, prob, modes,
-                                  best, dev, stream, args)
+        line["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args)
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         recs, sample, cores = cpu_c3(w, 3, 1, target_s=0.5)
         m, _ = summarize_cpu(recs)
@@ -986,8 +985,7 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
     return res
 
 
-def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dsend, dC, out, prob, modes, best, dev,
-                stream, args):
+def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args):
     """The same metric end to end through the public API with the step's
     inputs in pinned host memory.  The GEMM chain copies A in, runs c3_gemm
     and reads C back; the collective reads its sources straight from the
