@@ -860,6 +860,11 @@ def main(argv=None):
     roof["kernel"] = "gemm_bf16_kernel (tcgen05)"
     roof["algorithmic_per_launch"] = w.gemm_bytes if roof["bound"] == "hbm" else w.gemm_flops
     roof["peak_source"] = f"{peaks['source']} (burst)"
+    l2_bytes = info.get("l2_bytes") or 0
+    if w.gemm_bytes < l2_bytes:
+        roof["regime"] = (f"launch-latency bound: operands and output ({w.gemm_bytes / 1e6:.1f} MB) fit in the "
+                          f"{l2_bytes / 1e6:.0f} MB L2 and one launch lasts {1e6 * tg_mean:.1f} us, so the "
+                          f"fraction of the peak says little here")
     tc_sm = step_mean([r["t_comm_iso"] for r in per_mode["baseline"]]) if "baseline" in per_mode else None
     copy_roof = None
     if tc_sm and host_src:
@@ -874,6 +879,9 @@ def main(argv=None):
                      "frac": gbs / peaks["hbm_gbs"],
                      "kernel": ("reduce_scatter_kernel + copy_vec_kernel" if w.coll == "allreduce"
                                 else "copy_vec_kernel") + " (default budget)"}
+        if w.coll_traffic_bytes < l2_bytes:
+            copy_roof["regime"] = (f"launch-latency bound: the collective moves {w.coll_traffic_bytes / 1e6:.1f} MB, "
+                                   f"less than the L2 holds, in {1e6 * tc_sm:.1f} us")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
