@@ -72,8 +72,13 @@ constexpr int kGraphCache = 16;
 static GraphEntry g_graphs[kGraphCache];
 static unsigned long long g_graph_clock = 0;
 
+// The whole table is the key: the layout (kind, ranks) decides how the
+// captured graph issues the copies, and the source's memory type how the
+// driver carries them.
 static bool same_table(const SegTable& a, const SegTable& b) {
-    if (a.nseg != b.nseg || a.seg_bytes != b.seg_bytes) return false;
+    if (a.nseg != b.nseg || a.seg_bytes != b.seg_bytes || a.kind != b.kind || a.nranks != b.nranks ||
+        a.host_src != b.host_src)
+        return false;
     for (int i = 0; i < a.nseg; ++i)
         if (a.src[i] != b.src[i] || a.dst[i] != b.dst[i]) return false;
     return true;
