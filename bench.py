@@ -5,10 +5,12 @@ one GB300, in every mode the library offers, against the ideal speedup.
 One step = one pass of the whole path for every mode: for each mode, the GEMM
 alone, the collective alone (on that mode's engine), the two in series, and
 the two concurrently in the mode (the C3 timer, ``c3_time`` with one
-repetition), L2 flushed before each phase.  The workload is the memory-bound
-C3 case: GEMM M=256, N=28672, K=8192 (bf16, N(0,1) activations, N(0,0.02)
-weights, fp32 out) with an all-gather of an 8192x8192 bf16 weight from 8
-virtual ranks (8 x 16 MiB).
+repetition), L2 flushed before each phase.  The default workload is the
+largest C3 case: the Llama-405B-shaped GEMM M=8192, N=53248, K=16384 (bf16,
+N(0,1) activations, N(0,0.02) weights, fp32 out) beside an 8x8 all-to-all of
+8 MiB blocks (512 MiB of random bf16 payload), with the copy kernel on all
+SMs, partitioned onto 8/16/32 SMs, and offloaded to the driver's memcpy path.
+``--workload`` selects the others (``mem_ag``, ``ffn70_ag``, ...).
 
 value = realized share of the ideal C3 gain, (S_real - 1) / (S_ideal - 1), of
 the best mode, from the means over the timed steps (S_ideal = (T_g + T_c) /
@@ -18,6 +20,9 @@ a mode cannot look better by having a slow collective of its own; the share
 against the mode's own engine is reported beside it.  Means, as the pages
 average their runs: CUDA event times on GB300 come in steps of about 2 us, so a
 median snaps to a step while the mean over many steps resolves below one.
+
+Output: detail lines first (every mode's statistics, the kernel rates beside
+the C3 line, the end-to-end variants), then ONE compact headline line, last.
 
 ``--impl reference`` times the CPU oracle on the same workload (a bounded
 sample of it) through the same C3 procedure; it is the reference arm.
@@ -45,7 +50,7 @@ if ROOT not in sys.path:
 
 METRIC = "realized % of ideal C3 speedup; GEMM TFLOP/s + copy GB/s under overlap"
 UNIT = "% of ideal C3 gain"
-WORKLOAD = "mem_ag"
+WORKLOAD = "l405_a2a"
 
 # (name, mode, sm_split, priority).  Pages' names: c3_base, c3_sp, c3_rp (best
 # power-of-two split, oracle-selected), sp+rp, ConCCL, ConCCL_rp; reclaim_k is
@@ -65,6 +70,27 @@ MODES = [
     ("ce_rp_16", 2, 16, 0),
 ]
 
+# Modes a workload runs by default (every mode otherwise).  The Llama-405B
+# pair names its own set: the copy kernel on every SM, on 8/16/32 SMs, and
+# the copy-engine path with and without SMs taken from the GEMM; the
+# prioritised launch and the partition with reclaim ride along.
+DEFAULT_MODES = {
+    "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_16",
+                 "ce", "ce_rp_8"],
+}
+
+
+def select_modes(workload, names=""):
+    """The (name, mode, split, priority) tuples a run times: `names` (comma
+    separated) if given, else the workload's default set, else every mode."""
+    wanted = names.split(",") if names else DEFAULT_MODES.get(workload)
+    if not wanted:
+        return list(MODES)
+    unknown = [n for n in wanted if n not in {m[0] for m in MODES}]
+    if unknown:
+        raise SystemExit(f"unknown mode(s) {unknown}: one of {[m[0] for m in MODES]}")
+    return [m for m in MODES if m[0] in wanted]
+
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -75,6 +101,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD,
                     help="a named workload, or a size-sweep point such as sweep_allgather_4194304k")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0,
+                    help="timed steps of the end-to-end measurement (0: --steps, capped to about 30 s of work)")
+    ap.add_argument("--detail-out", default=None,
+                    help="also append the detail records (per-mode statistics, aux, e2e) to this file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--modes", default="", help="comma-separated subset of mode names")
     ap.add_argument("--no-aux", action="store_true", help="skip the compute-bound GEMM and copy-budget sweeps")
@@ -145,14 +175,23 @@ def expected_collective(np, w, payload):
     return np.tile(acc, len(payload)).view(np.uint8)
 
 
-def gemm_rows_reference(np, A_bits, B_bits, rows):
+def gemm_rows_reference(np, A_bits, B_bits, rows, chunk=4096):
     """Exact values and tolerances of sampled GEMM rows: the bf16 operands
     widened exactly, products and sums in fp64 (numpy); the tolerance is
-    1e-4 * sum_k |a b|."""
+    1e-4 * sum_k |a b|.  B is widened `chunk` rows at a time, so a 53248 x
+    16384 weight never exists in fp64 all at once."""
     def widen(u16):
         return (np.asarray(u16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    A, B = widen(A_bits[rows]), widen(B_bits)
-    return A @ B.T, 1e-4 * (np.abs(A) @ np.abs(B).T)
+    A = widen(A_bits[rows])
+    N = B_bits.shape[0]
+    ref = np.empty((A.shape[0], N), np.float64)
+    bound = np.empty((A.shape[0], N), np.float64)
+    absA = np.abs(A)
+    for n0 in range(0, N, chunk):
+        Bc = widen(B_bits[n0:n0 + chunk])
+        ref[:, n0:n0 + chunk] = A @ Bc.T
+        bound[:, n0:n0 + chunk] = 1e-4 * (absA @ np.abs(Bc).T)
+    return ref, bound
 
 
 def gemm_rows_ok(np, A_bits, B_bits, rows, C_rows, reference=None):
@@ -687,7 +726,7 @@ def main(argv=None):
     if args.heuristics:
         return run_heuristics(args, c3, torch, np, I, dev, info)
     w = find_workload(I, args.workload)
-    modes = MODES if not args.modes else [m for m in MODES if m[0] in args.modes.split(",")]
+    modes = select_modes(w.name, args.modes)
 
     # ---- inputs (host-generated, seeded), resident in HBM before timing
     A_h, B_h = I.gemm_operands(w)
@@ -852,14 +891,18 @@ def main(argv=None):
         achieved = w.gemm_bytes / tg_mean / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
+        roof["peak_source"] = f"{peaks['source']} copy bandwidth"
     else:
+        # the GEMM-alone phases run inside the continuous timed region, seconds of
+        # back-to-back work under the power cap: the sustained tensor peak applies
         achieved = w.gemm_flops / tg_mean / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"]}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peaks['source']} bf16, sustained (timed inside the continuous step)"}
     roof["traffic"] = profiled_traffic(w.name)
     roof["kernel"] = "gemm_bf16_kernel (tcgen05)"
     roof["algorithmic_per_launch"] = w.gemm_bytes if roof["bound"] == "hbm" else w.gemm_flops
-    roof["peak_source"] = f"{peaks['source']} (burst)"
     l2_bytes = info.get("l2_bytes") or 0
     if w.gemm_bytes < l2_bytes:
         roof["regime"] = (f"launch-latency bound: operands and output ({w.gemm_bytes / 1e6:.1f} MB) fit in the "
@@ -883,22 +926,22 @@ def main(argv=None):
             copy_roof["regime"] = (f"launch-latency bound: the collective moves {w.coll_traffic_bytes / 1e6:.1f} MB, "
                                    f"less than the L2 holds, in {1e6 * tc_sm:.1f} us")
 
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    detail = {
+        "detail": "c3", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.description}", "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": w.name, "description": w.description, "M": w.M, "N": w.N, "K": w.K,
                    "collective": f"{w.coll} {w.nranks} ranks x {w.unit_bytes} B",
                    "l2": f"flushed before every timed phase ({flush.numel() >> 20} MiB zero-fill, then its first "
                          f"half read back so L2 holds clean lines)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "coll_l2": args.coll_l2, "ce_variant": args.ce_variant,
-                   "coll_src": ("page-locked host memory (remote ranks across the CPU-GPU link)" if host_src
-                                else "device memory (8 emulated ranks in one HBM)"),
+                   "coll_src": "host" if host_src else "device",
                    "modes": [m[0] for m in modes]},
         "best_mode": best,
         # rank 0's replica: bootstrap over its timed steps
         "value_ci95": stats[best]["pct_ideal_gain_ci95"],
+        "class": stats[best]["class"],
         "gemm_tflops_overlap": stats[best]["gemm_tflops_overlap"],
         "copy_gbs_overlap": stats[best]["copy_gbs_overlap"],
         "roofline": roof, "roofline_copy": copy_roof,
@@ -911,22 +954,104 @@ def main(argv=None):
         "modes": stats,
         "device": {"name": torch.cuda.get_device_name(dev), **info},
     }
-    line["clocks"] = clk.summary()
+    detail["clocks"] = clk.summary()
+    if rank == 0:
+        emit_detail(detail, args.detail_out)
 
     if not args.no_aux:
-        line["aux"] = aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info)
+        detail["aux"] = aux_measure(c3, torch, w, dev, stream, peaks, dshards, dsend, out, info)
+        if rank == 0:
+            emit_detail({"detail": "aux", **detail["aux"]}, args.detail_out)
     if not args.no_e2e:
-        line["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args)
+        detail["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args)
+        if rank == 0:
+            emit_detail({"detail": "e2e", **detail["e2e"]}, args.detail_out)
     if not args.no_cpu_baseline and world == 1 and rank == 0:
         recs, sample, cores = cpu_c3(w, 3, 1, target_s=0.5)
         m, _ = summarize_cpu(recs)
-        line["cpu_baseline"] = {"value": m["pct_ideal_gain"], "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        detail["cpu_baseline"] = {"value": m["pct_ideal_gain"], "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": sample}
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(headline_line(detail)), flush=True)
     if pg is not None:
         pg.destroy_process_group()
     return 0
+
+
+def emit_detail(obj, path=None):
+    """One detail record: a JSON line on stdout (before the headline line),
+    and appended to `path` when given."""
+    text = json.dumps(obj)
+    print(text, flush=True)
+    if path:
+        with open(path, "a") as fh:
+            fh.write(text + "\n")
+
+
+HEADLINE_MAX_BYTES = 2048
+
+
+def _sig(x, digits=5):
+    """Floats rounded to `digits` significant digits (recursively), so the
+    headline stays short; other values unchanged."""
+    if isinstance(x, float):
+        if x != x or x in (float("inf"), float("-inf")):
+            return None
+        return float(f"{x:.{digits}g}")
+    if isinstance(x, dict):
+        return {k: _sig(v, digits) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [_sig(v, digits) for v in x]
+    return x
+
+
+def headline_line(d):
+    """The one compact JSON line the run ends with (under HEADLINE_MAX_BYTES):
+    the headline value and its interval, every mode's share, the roofline of
+    the dominant kernel and of the copy, the CPU baseline, the end-to-end
+    number, clocks, launches and the validation verdicts.  Everything else is
+    in the detail lines printed before it."""
+    roof = d.get("roofline") or {}
+    croof = d.get("roofline_copy") or {}
+    e2e = d.get("e2e")
+    cfg = d["config"]
+    line = {
+        "metric": d["metric"], "value": d["value"], "unit": d["unit"], "n_gpus": d["n_gpus"], "steps": d["steps"],
+        "warmup": d["warmup"], "ms_per_step": d["ms_per_step"], "higher_is_better": d["higher_is_better"],
+        "scaling": d["scaling"], "vs_baseline": d["vs_baseline"], "dtype": d["dtype"], "data": d["data"],
+        "config": {"workload": cfg["workload"], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
+                   "collective": cfg["collective"], "coll_src": cfg["coll_src"],
+                   "l2": "flushed before every timed phase (2 x L2 zero-fill)",
+                   "parallelism": cfg["parallelism"]},
+        "best_mode": d["best_mode"], "value_ci95": d.get("value_ci95"),
+        "modes_pct": {k: v["pct_ideal_gain"] for k, v in d.get("modes", {}).items()},
+        "class": d.get("class"),
+        "gemm_tflops_overlap": d.get("gemm_tflops_overlap"), "copy_gbs_overlap": d.get("copy_gbs_overlap"),
+        "roofline": {k: roof.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "traffic",
+                                               "algorithmic_per_launch", "kernel", "peak_source") if k in roof},
+        "roofline_copy": ({k: croof.get(k) for k in ("bound", "achieved", "peak", "unit", "frac", "kernel")}
+                          if croof else None),
+        "gpu_launches": d.get("gpu_launches"),
+        "validation": {k: d["validation"][k] for k in ("collective_bit_exact", "gemm_rows_in_tolerance")},
+        "clocks": d.get("clocks"),
+    }
+    for key in ("gemm_bound", "coll_bound"):
+        if key in d:
+            line[key] = d[key]
+    if d.get("cpu_baseline"):
+        line["cpu_baseline"] = d["cpu_baseline"]
+    if e2e:
+        line["e2e"] = {k: e2e.get(k) for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step",
+                                                "engine", "mode")}
+    line = _sig(line)
+    # stay under the cap whatever the strings hold: drop the least needed keys first
+    for key in ("modes_pct", "roofline_copy", "clocks"):
+        if len(json.dumps(line)) <= HEADLINE_MAX_BYTES:
+            break
+        line.pop(key, None)
+    if len(json.dumps(line)) > HEADLINE_MAX_BYTES and "cpu_baseline" in line:
+        line["cpu_baseline"]["sample"] = line["cpu_baseline"]["sample"][:160]
+    return line
 
 
 def _event_time(torch, stream, fn, reps, warm, flush=None):
@@ -947,7 +1072,7 @@ def _event_time(torch, stream, fn, reps, warm, flush=None):
     return statistics.fmean(ts), ts
 
 
-def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
+def aux_measure(c3, torch, w, dev, stream, peaks, dshards, dsend, out, info):
     """Isolated kernel rates beside the C3 line: the GEMM on the compute-bound
     shapes of the other workloads (TFLOP/s vs the dense bf16 peak), and the
     collective's GB/s per SM budget for both SM kernels and the driver memcpy
@@ -967,15 +1092,21 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
         res["gemm"][f"{M}x{N}x{K}"] = {"us": 1e6 * t, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
                                         "plan": list(c3.c3_gemm_plan(M, N, K, 0))}
         del A, B, C
-    if dshards is not None and w.coll == "allgather":
+    copies = w.coll in ("allgather", "alltoall") and (dshards is not None or dsend is not None)
+    if copies:
         nbytes = 2 * w.coll_bytes
+        cid = c3.C3_COLL_ALLGATHER if w.coll == "allgather" else c3.C3_COLL_ALLTOALL
+
+        def coll_only(**kw):
+            # the collective alone: a problem with an empty GEMM, run through c3_run
+            # (serial mode), which carries the flavour and SM budget
+            return c3.Problem(None, None, None, 0, 0, 0, cid, out, w.unit_bytes, w.nranks, shards=dshards,
+                              send=dsend, stream=stream, **kw)
+
         for kind, smk in (("vec", c3.C3_SMK_VEC), ("bulk", c3.C3_SMK_BULK)):
             res["copy_gbs_by_sms"][kind] = {}
             for k in (8, 16, 32, 64, 96, info["sm_count"]):
-                # c3_allgather has no flavour switch, so the collective runs through
-                # c3_run (serial mode) with an empty GEMM and the flavour in the record.
-                prob = c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLGATHER, out, w.unit_bytes, w.nranks,
-                                  shards=dshards, comm_sms=k, sm_kernel=smk, stream=stream)
+                prob = coll_only(comm_sms=k, sm_kernel=smk)
                 tl = []
                 for _ in range(6):
                     do_flush()
@@ -985,9 +1116,7 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, out, info):
         tl = []
         for _ in range(6):
             do_flush()
-            tl.append(c3.c3_run(c3.Problem(None, None, None, 0, 0, 0, c3.C3_COLL_ALLGATHER, out, w.unit_bytes,
-                                           w.nranks, shards=dshards, stream=stream),
-                                c3.C3_MODE_SERIAL_CE, 0, 0)["t_conc"])
+            tl.append(c3.c3_run(coll_only(), c3.C3_MODE_SERIAL_CE, 0, 0)["t_conc"])
         res["copy_gbs_by_sms"]["ce"] = nbytes / statistics.median(tl[1:]) / 1e9
         res["copy_gbs_by_sms"]["peak_hbm_gbs"] = peaks["hbm_gbs"]
     return res
@@ -1061,7 +1190,18 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, s
         stream.wait_event(done)
 
     tgs, tcs, tconcs = [], {e: [] for e in engines}, {v[0]: [] for v in variants}
-    for it in range(args.warmup + args.steps):
+    steps = args.e2e_steps
+    if steps <= 0:
+        # about 30 s of work at most: time one untimed pass of the step first
+        t0 = time.perf_counter()
+        timed(lambda e0: gemm_chain(stream))
+        for e in engines:
+            timed(lambda e0: coll_chain(stream, engines[e]))
+        for v, e, p in variants:
+            timed(lambda e0: conc(e0, engines[e], p))
+        per_step = time.perf_counter() - t0
+        steps = max(3, min(args.steps, int(30.0 / max(per_step, 1e-3))))
+    for it in range(args.warmup + steps):
         tg = timed(lambda e0: gemm_chain(stream))
         alone = {e: timed(lambda e0: coll_chain(stream, engines[e])) for e in engines}
         together = {v: timed(lambda e0: conc(e0, engines[e], p)) for v, e, p in variants}
@@ -1085,7 +1225,7 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, s
     best_v = max(per_variant, key=lambda v: per_variant[v]["pct_ideal_gain"])
     _, best_e, best_p = next(x for x in variants if x[0] == best_v)
     pe = per_variant[best_v]
-    return {"value": pe["pct_ideal_gain"], "unit": UNIT,
+    return {"value": pe["pct_ideal_gain"], "unit": UNIT, "steps": steps,
             # per step: A for the GEMM chain alone and in each of the 4 concurrent variants; the
             # payload for each engine's collective alone and in each concurrent variant; C back
             # after each GEMM chain

@@ -754,9 +754,13 @@ extern "C" int c3_gemm_noalloc(const void* A, const void* B, float* C, int64_t M
     // The static block records at most kCtaRecs CTAs: refuse a launch that would need more.
     if (plan.grid > kCtaRecs)
         return set_error(-5, "c3_gemm_noalloc: more than 256 CTAs would need more than its 16 KiB scratch");
-    // The block keeps the previous call's contents: clear it on this stream first.
+    // The block keeps the previous call's contents: clear it on this stream first,
+    // the scheduler slot this launch takes included (a launch that gave up a wait
+    // may have left its slot non-zero, and the status reset leaves slots alone).
     if ((rc = status_reset_launch(d->scratch, s))) return rc;
     unsigned int* sched = d->scratch->sched[d->next_sched++ % kSchedSlots];
+    cudaError_t ez = cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), s);
+    if (ez != cudaSuccess) return set_cuda_error(ez, "clearing the scheduler slot");
     if ((rc = launch_cfg(plan.ci, plan.grid, plan.ma, plan.mb, plan.mc, plan.has_mc, C, M, N, plan.num_m,
                          plan.num_n, plan.num_kb, sched, 1, d->scratch, s)))
         return rc;

@@ -352,8 +352,10 @@ int c3_time(const c3_problem *p, int mode, int sm_split, int priority, int warmu
  * The first call on each device does a one-time set-up with that device
  * current (looks up the array's device address, reads the SM count, sets the
  * kernels' shared-memory attribute); make that first call before any stream
- * capture.  Each call clears the scratch on `s` before the GEMM, since the
- * array keeps the previous call's contents.  All calls share the one array:
+ * capture.  Each call clears the scratch on `s` before the GEMM (the status
+ * words and the tile-scheduler slot it takes), since the array keeps the
+ * previous call's contents, also after a call whose wait gave up.  All calls
+ * share the one array:
  * calls whose executions overlap on the GPU (different streams, no ordering)
  * race on it, and a caller must order them.
  *   check  0: asynchronous on `s` (like c3_gemm); device wait timeouts are

@@ -126,3 +126,83 @@ def test_share_ci_covers_the_estimate_and_narrows_with_more_steps():
     w_few = bench.share_ci95(few, 42.0)
     w_many = bench.share_ci95(many, 42.0)
     assert (w_many[1] - w_many[0]) < 0.5 * (w_few[1] - w_few[0])      # ~1/sqrt(16) in theory
+
+
+def _synthetic_detail(n_modes=12, long_strings=False):
+    """A detail record shaped like the bench's, with every optional part."""
+    pad = "x" * (4000 if long_strings else 10)
+    modes = {f"mode_{i:02d}_{pad[:20]}": {"pct_ideal_gain": 12.3456789 + i, "other": list(range(50))}
+             for i in range(n_modes)}
+    return {
+        "detail": "c3", "metric": bench.METRIC, "value": 19.87654321, "unit": bench.UNIT, "n_gpus": 1,
+        "steps": 20, "warmup": 5, "ms_per_step": 312.123456789, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "l405_a2a", "description": pad, "M": 8192, "N": 53248, "K": 16384,
+                   "collective": "alltoall 8 ranks x 8388608 B", "l2": pad, "parallelism": "single GPU",
+                   "coll_l2": "normal", "ce_variant": "graph", "coll_src": "device", "modes": list(modes)},
+        "best_mode": "baseline", "value_ci95": [10.123456, 29.987654], "class": "G-long",
+        "gemm_bound": "compute", "coll_bound": "bandwidth",
+        "gemm_tflops_overlap": 1650.123456, "copy_gbs_overlap": 3100.98765,
+        "roofline": {"bound": "tensor", "achieved": 1650.1, "peak": 1706.7, "unit": "TFLOP/s", "frac": 0.96681,
+                     "frac_of_burst": 0.9, "traffic": 1.2345678e10, "algorithmic_per_launch": 1.4293e13,
+                     "kernel": "gemm_bf16_kernel (tcgen05)", "peak_source": "measured bf16, sustained " + pad[:40]},
+        "roofline_copy": {"bound": "hbm", "achieved": 5900.0, "peak": 6781.4, "unit": "GB/s", "frac": 0.87,
+                          "kernel": "copy_vec_kernel (default budget)", "regime": pad},
+        "gpu_launches": 123456,
+        "validation": {"collective_bit_exact": True, "gemm_rows_in_tolerance": True,
+                       "per_mode": {k: {"collective_bit_exact": True} for k in modes}, "gemm_rows": [0, 1, 2, 3]},
+        "modes": modes, "device": {"name": "NVIDIA GB300", "sm_count": 152},
+        "clocks": {"sm_mhz": 1455.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 300},
+        "aux": {"gemm": {f"s{i}": {"us": 1.0 * i} for i in range(100)}},
+        "e2e": {"value": 55.5, "unit": bench.UNIT, "h2d_bytes_per_step": 826277888, "d2h_bytes_per_step": 146800640,
+                "engine": "memcpy", "mode": "baseline", "variants": {f"v{i}": pad for i in range(8)}},
+        "cpu_baseline": {"value": 3.25, "unit": bench.UNIT, "cores": 16, "kind": "oracle",
+                         "sample": "28 of 8192 rows of A against all 53248x16384 of B " + pad[:200]},
+    }
+
+
+@pytest.mark.parametrize("n_modes,long_strings", [(8, False), (12, False), (40, True)])
+def test_headline_line_is_compact_and_parses(n_modes, long_strings):
+    import json
+    line = bench.headline_line(_synthetic_detail(n_modes, long_strings))
+    text = json.dumps(line)
+    assert len(text) <= bench.HEADLINE_MAX_BYTES
+    back = json.loads(text)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "dtype", "config", "best_mode", "value_ci95", "roofline", "cpu_baseline", "e2e", "gpu_launches",
+                "validation"):
+        assert key in back, key
+    assert back["config"]["workload"] == "l405_a2a"
+    assert back["roofline"]["frac"] == pytest.approx(0.96681)
+    assert back["e2e"]["h2d_bytes_per_step"] == 826277888
+    assert set(back["validation"]) == {"collective_bit_exact", "gemm_rows_in_tolerance"}
+    assert "modes" not in back and "aux" not in back and "detail" not in back
+
+
+def test_headline_line_keeps_every_mode_share_when_it_fits():
+    import json
+    d = _synthetic_detail(8)
+    line = bench.headline_line(d)
+    assert set(line["modes_pct"]) == set(d["modes"])
+    assert len(json.dumps(line)) <= bench.HEADLINE_MAX_BYTES
+    assert line["value"] == pytest.approx(19.877, rel=1e-4)       # 5 significant digits
+
+
+def test_default_modes_of_the_405b_pair_and_explicit_subsets():
+    names = [m[0] for m in bench.select_modes("l405_a2a")]
+    for n in ("baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "ce", "ce_rp_8"):
+        assert n in names
+    assert [m[0] for m in bench.select_modes("mem_ag")] == [m[0] for m in bench.MODES]
+    assert [m[0] for m in bench.select_modes("l405_a2a", "ce,baseline")] == ["baseline", "ce"]
+    with pytest.raises(SystemExit):
+        bench.select_modes("mem_ag", "no_such_mode")
+
+
+def test_gemm_rows_reference_in_chunks_equals_one_pass():
+    w = I.WORKLOADS["tiny_ag"]
+    A, B = I.gemm_operands(w)
+    rows = np.array([3, 100, 511])
+    ref1, b1 = bench.gemm_rows_reference(np, A, B, rows, chunk=1 << 20)
+    ref2, b2 = bench.gemm_rows_reference(np, A, B, rows, chunk=97)      # ragged last chunk
+    # the same fp64 dot products; a BLAS may block K differently per shape, so allow its last bits
+    assert np.allclose(ref1, ref2, rtol=1e-12, atol=1e-12) and np.allclose(b1, b2, rtol=1e-12, atol=0)

@@ -2,10 +2,17 @@
 (code running under a host framework that owns a fixed memory pool, a plugin
 invoked while its caller holds the whole device, real-time code that may not
 enter the allocator).  Its scratch lives in a static device array inside
-libc3.so, so it must give the same C as c3_gemm, call after call, without the
-library's per-device state.  This file is collected last on purpose: if it
-fails, a run that stops at the first failure has already run every other test.
+libc3.so.  These tests hold its output to the oracle, call after call, and
+check in a fresh process that it works as the library's very first call and
+that repeated calls take no device memory.  This file is collected last on
+purpose: if it fails, a run that stops at the first failure has already run
+every other test.
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -16,29 +23,74 @@ from concurrent_communication_overlap_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4  # the GEMM tolerance of every other test: |err| <= 1e-4 * sum_k |a*b|
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (M, N, K, sm_budget): the second call has ragged edges and a capped grid
+SHAPES = [(512, 768, 512, 0), (300, 200, 264, 5)]
 
 
-def test_noalloc_gemm_matches_c3_gemm_two_calls_in_a_row():
+def _operands(call, M, N, K):
+    return I.bf16_uniform(2000 + call, (M, K), -1.0, 1.0), I.bf16_uniform(3000 + call, (N, K), -1.0, 1.0)
+
+
+def _within_oracle(got, A, B):
+    C_ref, S = oracle.gemm(A, B)
+    return bool(np.isfinite(got).all() and (np.abs(got.astype(np.float64) - C_ref) <= TOL * S).all())
+
+
+def test_noalloc_gemm_matches_the_oracle_two_calls_in_a_row():
     from concurrent_communication_overlap_gb300 import c3
-    shapes = [(512, 768, 512, 0), (300, 200, 264, 5)]   # second call: ragged edges, capped grid
-    for call, (M, N, K, budget) in enumerate(shapes):
-        A = I.bf16_uniform(2000 + call, (M, K), -1.0, 1.0)
-        B = I.bf16_uniform(3000 + call, (N, K), -1.0, 1.0)
+    for call, (M, N, K, budget) in enumerate(SHAPES):
+        A, B = _operands(call, M, N, K)
         dA = torch.from_numpy(A.view(np.int16)).cuda()
         dB = torch.from_numpy(B.view(np.int16)).cuda()
-        c_noalloc = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-        c_ref = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
-        # the allocation-free entry point first: in a fresh process this is its first call
-        assert c3.c3_gemm_noalloc(dA, dB, c_noalloc, M, N, K, budget, sync_check=True, check=False) == c3.C3_OK, \
+        assert c3.c3_gemm_noalloc(dA, dB, dC, M, N, K, budget, sync_check=True, check=False) == c3.C3_OK, \
             c3.c3_last_error()
-        c3.c3_gemm(dA, dB, c_ref, M, N, K, budget)
-        c3.c3_status_check()
-        got = c_noalloc.cpu().numpy().astype(np.float64)
-        ref = c_ref.cpu().numpy().astype(np.float64)
-        _, S = oracle.gemm(A, B)
-        assert not np.isnan(got).any()
-        assert (np.abs(got - ref) <= TOL * S).all(), call
+        assert _within_oracle(dC.cpu().numpy(), A, B), call
+
+
+# Run in a child process: c3_gemm_noalloc is the first call into libc3 there,
+# and the free device memory is read before and after the later calls.
+_CHILD = r"""
+import json, sys
+import numpy as np
+import torch
+sys.path.insert(0, sys.argv[1])
+from concurrent_communication_overlap_gb300 import c3
+from concurrent_communication_overlap_gb300 import inputs as I
+shapes = json.loads(sys.argv[2])
+bufs = []
+for call, (M, N, K, budget) in enumerate(shapes):
+    A = I.bf16_uniform(2000 + call, (M, K), -1.0, 1.0)
+    B = I.bf16_uniform(3000 + call, (N, K), -1.0, 1.0)
+    bufs.append((torch.from_numpy(A.view(np.int16)).cuda(), torch.from_numpy(B.view(np.int16)).cuda(),
+                 torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")))
+torch.cuda.synchronize()
+rcs, free = [], []
+for rep in range(3):                      # call 1 does the one-time set-up; calls 2-3 must allocate nothing
+    for (M, N, K, budget), (dA, dB, dC) in zip(shapes, bufs):
+        rcs.append(c3.c3_gemm_noalloc(dA, dB, dC, M, N, K, budget, sync_check=True, check=False))
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+out = [dC.cpu().numpy().tolist() for (_, _, dC) in bufs]
+print(json.dumps({"rcs": rcs, "free": free, "out": out, "err": c3.c3_last_error()}))
+"""
+
+
+def test_noalloc_first_call_in_a_fresh_process_allocates_nothing():
+    env = dict(os.environ)
+    res = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(SHAPES)], capture_output=True, text=True,
+                         timeout=600, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    assert all(rc == 0 for rc in d["rcs"]), d["err"]
+    # free device memory after the first round of calls is unchanged by the next two
+    assert d["free"][1] == d["free"][0] and d["free"][2] == d["free"][0], d["free"]
+    for call, (M, N, K, _) in enumerate(SHAPES):
+        A, B = _operands(call, M, N, K)
+        assert _within_oracle(np.asarray(d["out"][call], dtype=np.float32), A, B), call
 
 
 def test_noalloc_rejects_bad_arguments_without_launching():
