@@ -57,6 +57,8 @@ def _load():
             lib.oracle_reduce_scatter_f32.restype = ctypes.c_int
             lib.oracle_c3_metrics.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double, dp,
                                               ctypes.POINTER(ctypes.c_int)]
+            lib.oracle_c3_bounds.argtypes = [ctypes.c_double] * 7 + [ctypes.POINTER(ctypes.c_int)] * 2
+            lib.oracle_c3_bounds.restype = ctypes.c_int
             for f in (lib.oracle_gemm, lib.oracle_gemm_entries, lib.oracle_allgather,
                       lib.oracle_alltoall, lib.oracle_c3_metrics):
                 f.restype = ctypes.c_int
@@ -189,3 +191,22 @@ def c3_metrics(t_gemm, t_comm, t_conc):
         raise ValueError(f"oracle_c3_metrics rc={rc}")
     return {"s_ideal": out[0], "s_real": out[1], "pct_ideal_gain": out[2], "pct_ideal_ratio": out[3],
             "t_serial": out[4], "t_ideal": out[5], "class": CLASS_NAMES[cls.value]}
+
+
+GEMM_BOUND_NAMES = {-1: "unknown", 0: "compute", 1: "memory"}
+COLL_BOUND_NAMES = {-1: "unknown", 0: "latency", 1: "bandwidth"}
+
+
+def c3_bounds(gemm_flops, gemm_bytes, peak_flops, peak_bytes_per_s, coll_bytes, t_comm, plateau_bytes_per_s):
+    """The taxonomy's other two axes: ("compute" | "memory" | "unknown",
+    "latency" | "bandwidth" | "unknown").  Memory-bound GEMM when
+    flops / bytes < peak_flops / peak_bytes_per_s; bandwidth-bound collective
+    when coll_bytes / t_comm >= plateau / 2.  A peak or plateau <= 0 gives
+    "unknown" on its axis."""
+    g, c = ctypes.c_int(), ctypes.c_int()
+    rc = _load().oracle_c3_bounds(float(gemm_flops), float(gemm_bytes), float(peak_flops), float(peak_bytes_per_s),
+                                  float(coll_bytes), float(t_comm), float(plateau_bytes_per_s), ctypes.byref(g),
+                                  ctypes.byref(c))
+    if rc:
+        raise ValueError(f"oracle_c3_bounds rc={rc}")
+    return GEMM_BOUND_NAMES[g.value], COLL_BOUND_NAMES[c.value]

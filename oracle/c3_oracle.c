@@ -46,6 +46,13 @@
  *       T_concurrent, the share of the ideal gain realized, the plain ratio,
  *       and the taxonomy class with the 115% / 15% thresholds (Section III).
  *
+ *   oracle_c3_bounds
+ *       the taxonomy's other two axes: compute- or memory-bound GEMM (its
+ *       arithmetic intensity against the roofline ridge) and latency- or
+ *       bandwidth-bound collective (its isolated rate against half the
+ *       plateau of a size sweep, the threshold the referee asks for on
+ *       Section III).
+ *
  * Every function returns 0 on success and a negative value on bad arguments.
  */
 #include <math.h>
@@ -246,5 +253,41 @@ int oracle_c3_metrics(double t_gemm, double t_comm, double t_conc, double *out, 
         *cls = ORACLE_C_LONG;
     else
         *cls = ORACLE_GC_EQUAL;
+    return 0;
+}
+
+/* The taxonomy's other two axes (the pith.science verdict's summary of the
+ * paper: "compute-bound versus memory-bound GEMMs; latency-bound versus
+ * bandwidth-bound collectives"; Section III).
+ *
+ * GEMM: the roofline reading.  Its arithmetic intensity I = flops / bytes is
+ * set against the machine's ridge P / W (peak FLOP/s over peak bytes/s); the
+ * GEMM is memory-bound when I < P / W and compute-bound otherwise.  Compared
+ * cross-multiplied, flops * W < bytes * P, so no ratio is rounded.
+ *
+ * Collective: the paper calls a collective latency-bound when its time does
+ * not grow in proportion to its size, and the referee's minor comment on
+ * Section III asks for a bandwidth-plateau threshold instead.  The reading
+ * here: bandwidth-bound when the isolated rate coll_bytes / t_comm reaches
+ * half of the plateau rate of the same engine's size sweep, i.e.
+ * 2 * coll_bytes >= plateau * t_comm; latency-bound below.
+ *
+ * A bound whose inputs are missing (a peak or the plateau <= 0) is -1.
+ * *gemm_bound: 0 compute-bound, 1 memory-bound.  *coll_bound: 0 latency-bound,
+ * 1 bandwidth-bound.  Returns -1 on null outputs or non-positive sizes/times. */
+int oracle_c3_bounds(double gemm_flops, double gemm_bytes, double peak_flops, double peak_bytes_per_s,
+                     double coll_bytes, double t_comm, double plateau_bytes_per_s, int *gemm_bound,
+                     int *coll_bound)
+{
+    if (!gemm_bound || !coll_bound) return -1;
+    if (!(gemm_flops > 0.0) || !(gemm_bytes > 0.0) || !(coll_bytes > 0.0) || !(t_comm > 0.0)) return -1;
+    if (peak_flops > 0.0 && peak_bytes_per_s > 0.0)
+        *gemm_bound = (gemm_flops * peak_bytes_per_s < gemm_bytes * peak_flops) ? 1 : 0;
+    else
+        *gemm_bound = -1;
+    if (plateau_bytes_per_s > 0.0)
+        *coll_bound = (2.0 * coll_bytes >= plateau_bytes_per_s * t_comm) ? 1 : 0;
+    else
+        *coll_bound = -1;
     return 0;
 }

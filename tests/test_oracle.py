@@ -331,3 +331,28 @@ def test_reduce_scatter_keeps_only_own_chunk():
         mask = np.ones(n, bool)
         mask[own] = False
         assert np.all(out[r, mask] == -7.0)
+
+
+def test_c3_taxonomy_bounds_golden_rows():
+    for row in load_rows("taxonomy_bounds.txt"):
+        if row[0] == "gemm":
+            flops, nbytes, pf, pw = map(float, row[1:5])
+            g, _ = oracle.c3_bounds(flops, nbytes, pf, pw, 1.0, 1.0, 1.0)
+            assert g == row[5], row
+        else:
+            cb, t, plat = map(float, row[1:4])
+            _, c = oracle.c3_bounds(1.0, 1.0, 1.0, 1.0, cb, t, plat)
+            assert c == row[4], row
+
+
+def test_c3_taxonomy_bounds_follow_the_stated_ratios():
+    # the GEMM axis moves with the arithmetic intensity, not with flops or bytes alone
+    assert oracle.c3_bounds(1e12, 1e10, 1e15, 1e13, 1, 1, 1)[0] == "compute"     # I = 100 = ridge
+    assert oracle.c3_bounds(1e12, 2e10, 1e15, 1e13, 1, 1, 1)[0] == "memory"      # I = 50 < 100
+    assert oracle.c3_bounds(2e12, 2e10, 1e15, 1e13, 1, 1, 1)[0] == "compute"     # I = 100 again
+    # the collective axis: halving the time at fixed size crosses into bandwidth-bound
+    assert oracle.c3_bounds(1, 1, 1, 1, 1e6, 4e-6, 1e12)[1] == "latency"          # 0.25 of plateau
+    assert oracle.c3_bounds(1, 1, 1, 1, 1e6, 1e-6, 1e12)[1] == "bandwidth"        # 1.0 of plateau
+    for bad in [(0, 1, 1, 1, 1, 1, 1), (1, 0, 1, 1, 1, 1, 1), (1, 1, 1, 1, 0, 1, 1), (1, 1, 1, 1, 1, 0, 1)]:
+        with pytest.raises(ValueError):
+            oracle.c3_bounds(*bad)
