@@ -101,6 +101,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=WORKLOAD,
                     help="a named workload, or a size-sweep point such as sweep_allgather_4194304k")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--settle-ms", type=float, default=-1.0,
+                    help="idle time before every timed phase, ms (-1: 2.5 x the isolated GEMM time, clamped to "
+                         "0.2 .. 20 ms); the GPU's power controller otherwise times phases in different clock states")
     ap.add_argument("--e2e-steps", type=int, default=0,
                     help="timed steps of the end-to-end measurement (0: --steps, capped to about 30 s of work)")
     ap.add_argument("--detail-out", default=None,
@@ -222,6 +225,34 @@ def c3_class(tg, tc):
     return "GC-equal"
 
 
+def most_common(xs):
+    """The most frequent value (the first seen among ties); None if empty."""
+    if not xs:
+        return None
+    counts = {}
+    for x in xs:
+        counts[x] = counts.get(x, 0) + 1
+    return max(counts, key=counts.get)
+
+
+def coll_bound_strict(per_mode, modes, plateaus, coll_bytes):
+    """Latency- or bandwidth-bound collective, for the strict T_comm: the
+    faster engine's mean isolated time against half of that engine's plateau
+    rate (the same rule as the library's c3_coll_bound)."""
+    by_engine = {}
+    for name, mode, split, prio in modes:
+        eng = "ce" if mode in (2, 3) else "sm"
+        by_engine.setdefault(eng, []).extend(r["t_comm_iso"] for r in per_mode[name])
+    means = {e: step_mean(v) for e, v in by_engine.items() if v}
+    if not means:
+        return None
+    eng = min(means, key=means.get)
+    plateau = plateaus.get(eng, 0.0)
+    if not plateau or means[eng] <= 0:
+        return "unknown"
+    return "bandwidth" if 2.0 * coll_bytes >= plateau * means[eng] else "latency"
+
+
 def step_mean(xs):
     """The per-step statistic every C3 time is summarised by: the mean over
     the timed steps (the pages average their runs; the event clock's ~2 us
@@ -239,16 +270,18 @@ def strict_comm_time(per_mode, modes):
     return min(step_mean(v) for v in by_engine.values() if v)
 
 
-def share_ci95(recs, tc_strict, n_boot=400, seed=0):
+def share_ci95(recs, tc_strict, n_boot=400, seed=0, tg_steps=None):
     """95% bootstrap interval of a mode's share of the ideal gain (percent):
     the timed steps are resampled with replacement and T_g and T_conc
-    re-averaged, with the strict T_c held at its full-sample mean.  Shows how
-    far step-to-step noise can move the share; it is wide wherever S_ideal - 1
-    is small.  None with fewer than 3 steps."""
+    re-averaged, with the strict T_c held at its full-sample mean.  T_g per
+    step is `tg_steps` (the step's GEMM-alone time pooled over the modes) when
+    given, else the mode's own.  Shows how far step-to-step noise can move the
+    share; it is wide wherever S_ideal - 1 is small.  None with fewer than 3
+    steps."""
     import numpy as np
     if len(recs) < 3 or not tc_strict or tc_strict <= 0:
         return None
-    tg = np.array([r["t_gemm_iso"] for r in recs], dtype=np.float64)
+    tg = np.array(tg_steps if tg_steps is not None else [r["t_gemm_iso"] for r in recs], dtype=np.float64)
     tconc = np.array([r["t_conc"] for r in recs], dtype=np.float64)
     idx = np.random.default_rng(seed).integers(0, len(recs), size=(n_boot, len(recs)))
     g, c = tg[idx].mean(axis=1), tconc[idx].mean(axis=1)
@@ -261,6 +294,26 @@ def share_ci95(recs, tc_strict, n_boot=400, seed=0):
     share = 100.0 * (s_real[ok] - 1.0) / (s_ideal[ok] - 1.0)
     lo, hi = np.percentile(share, [2.5, 97.5])
     return [float(lo), float(hi)]
+
+
+def auto_settle_us(t_gemm_s, settle_ms=-1.0):
+    """The idle period before each timed phase: `settle_ms` when given (>= 0),
+    else 2.5 x the isolated GEMM time clamped to 0.2 .. 20 ms.  Long enough for
+    the power controller to leave the previous phase's state: on the 7.4 ms
+    Llama-405B-shaped GEMM, 20 ms of idle cut the spread of its isolated time
+    from ~265 us (no gap) to ~50 us."""
+    if settle_ms is not None and settle_ms >= 0:
+        return int(round(1000.0 * settle_ms))
+    return int(round(1e6 * min(0.020, max(0.0002, 2.5 * t_gemm_s))))
+
+
+def pooled_gemm_times(per_mode):
+    """Per timed step, the mean of the isolated GEMM times that step took in
+    every mode.  The GEMM-alone phase is the same launch in every mode (all
+    SMs, nothing beside it), so its samples are pooled across modes."""
+    names = list(per_mode)
+    n = min(len(per_mode[k]) for k in names) if names else 0
+    return [statistics.fmean(per_mode[k][i]["t_gemm_iso"] for k in names) for i in range(n)]
 
 
 def spread(xs):
@@ -567,6 +620,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     dC = torch.empty((w0.M, w0.N), dtype=torch.float32, device=dev)
     flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    settle_us = None
     for w in ws:
         payload = I.coll_payload(w)
         if w.coll == "allgather":
@@ -576,9 +630,15 @@ def run_sweep(args, c3, torch, np, I, dev, info):
             dsh, dsend, cid = None, place(payload), c3.C3_COLL_ALLTOALL
             ref = expected_collective(np, w, payload)
         out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
+        if settle_us is None:
+            for _ in range(2):
+                c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
+            t_g0, _ = _event_time(torch, stream, lambda: c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream), 3, 0,
+                                  lambda: c3.c3_l2_flush(flush, flush.numel(), stream))
+            settle_us = auto_settle_us(t_g0, args.settle_ms)
         prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, cid, out, w.unit_bytes, w.nranks, shards=dsh, send=dsend,
                           flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
-                          ce_variant=ce_variant_arg(args, c3))
+                          ce_variant=ce_variant_arg(args, c3), settle_us=settle_us)
         per = {m[0]: [] for m in modes}
         for it in range(args.warmup + args.steps):
             for name, mode, split, prio in modes:
@@ -588,20 +648,22 @@ def run_sweep(args, c3, torch, np, I, dev, info):
         exact = bool(np.array_equal(out.cpu().numpy(), ref))
         res = {}
         tc_strict = strict_comm_time(per, modes)
+        tg_steps = pooled_gemm_times(per)
+        tg = step_mean(tg_steps)
         for name, recs in per.items():
-            tg = step_mean([r["t_gemm_iso"] for r in recs])
             tc = step_mean([r["t_comm_iso"] for r in recs])
             tconc = step_mean([r["t_conc"] for r in recs])
             m = pct_gain(tg, tc_strict, tconc)
             m_own = pct_gain(tg, tc, tconc)
             res[name] = {"t_gemm_us": 1e6 * tg, "t_comm_us": 1e6 * tc, "t_comm_strict_us": 1e6 * tc_strict,
                          "t_conc_us": 1e6 * tconc, "s_ideal": m["s_ideal"], "s_real": m["s_real"],
-                         "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_gain_ci95": share_ci95(recs, tc_strict),
+                         "pct_ideal_gain": m["pct_ideal_gain"],
+                         "pct_ideal_gain_ci95": share_ci95(recs, tc_strict, tg_steps=tg_steps),
                          "pct_ideal_ratio": m["pct_ideal_ratio"],
                          "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "class": c3_class(tg, tc_strict)}
         best = max(res, key=lambda k: res[k]["pct_ideal_gain"] if res[k]["s_ideal"] > 1.0 else -1e9)
         print(json.dumps({"sweep": args.sweep, "workload": w.name, "coll_bytes": w.coll_bytes, "steps": args.steps,
-                          "coll_src": args.coll_src,
+                          "coll_src": args.coll_src, "settle_us": settle_us,
                           "collective_bit_exact": exact, "best_mode": best, "modes": res}), flush=True)
         del out, dsh, dsend, prob
     return 0
@@ -752,9 +814,19 @@ def main(argv=None):
     out = torch.empty(w.coll_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+    # the settle period, from the GEMM's isolated time (after two untimed launches)
+    for _ in range(2):
+        c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
+    t_g0, _ = _event_time(torch, stream, lambda: c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream), 3, 0,
+                          lambda: c3.c3_l2_flush(flush, flush.numel(), stream))
+    settle_us = auto_settle_us(t_g0, args.settle_ms)
+    plateaus = {} if host_src else measure_plateaus(c3, torch, w, dev, stream, flush)
     prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
                       send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
-                          ce_variant=ce_variant_arg(args, c3))
+                      ce_variant=ce_variant_arg(args, c3), settle_us=settle_us,
+                      peak_flops=peaks["bf16_tflops"] * 1e12, peak_bytes_per_s=peaks["hbm_gbs"] * 1e9,
+                      coll_plateau_sm=plateaus.get("sm", 0.0), coll_plateau_ce=plateaus.get("ce", 0.0))
 
     if args.profile_range:
         # one profiled phase on the real workload buffers, after a few untimed runs
@@ -831,7 +903,6 @@ def main(argv=None):
     torch.cuda.synchronize(dev)
 
     # ---- statistics per mode (means over the timed steps)
-    peaks = load_peaks()
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     gemm_hbm_bound = w.gemm_flops / w.gemm_bytes < ridge
 
@@ -846,8 +917,11 @@ def main(argv=None):
     stats = {}
     all_tg = [r["t_gemm_iso"] for recs in per_mode.values() for r in recs]
     tc_strict = strict_comm_time(per_mode, modes)
+    # the GEMM-alone phase is the same launch in every mode: its mean over all
+    # modes' samples is every mode's T_g
+    tg_steps = pooled_gemm_times(per_mode)
+    tg = step_mean(tg_steps)
     for name, recs in per_mode.items():
-        tg = step_mean([r["t_gemm_iso"] for r in recs])
         tc = step_mean([r["t_comm_iso"] for r in recs])
         tconc = step_mean([r["t_conc"] for r in recs])
         m = pct_gain(tg, tc_strict, tconc)
@@ -861,12 +935,16 @@ def main(argv=None):
             "t_conc_us": 1e6 * tconc,
             "t_serial_meas_us": 1e6 * step_mean([r["t_serial_meas"] for r in recs]),
             "s_ideal": m["s_ideal"], "s_real": m["s_real"],
-            "pct_ideal_gain": m["pct_ideal_gain"], "pct_ideal_gain_ci95": share_ci95(recs, tc_strict),
+            "pct_ideal_gain": m["pct_ideal_gain"],
+            "pct_ideal_gain_ci95": share_ci95(recs, tc_strict, tg_steps=tg_steps),
+            "t_gemm_iso_own_us": 1e6 * step_mean([r["t_gemm_iso"] for r in recs]),
             "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
             "pct_ideal_gain_own_engine_per_step": spread([100.0 * r["pct_ideal_gain"] for r in recs]),
             "spread_us": {k: spread([1e6 * r[k] for r in recs]) for k in ("t_gemm_iso", "t_comm_iso", "t_conc")},
             "class": c3_class(tg, tc_strict), "class_own_engine": c3_class(tg, tc),
+            "gemm_bound": most_common([r["gemm_bound_name"] for r in recs]),
+            "coll_bound_own_engine": most_common([r["coll_bound_name"] for r in recs]),
             "gemm_tflops_overlap": w.gemm_flops / tgd / 1e12 if tgd > 0 else None,
             "copy_gbs_overlap": ((w.coll_bytes if host_src else w.coll_traffic_bytes) / step_mean(tcd) / 1e9
                                  if step_mean(tcd) > 0 else None),
@@ -942,6 +1020,10 @@ def main(argv=None):
         # rank 0's replica: bootstrap over its timed steps
         "value_ci95": stats[best]["pct_ideal_gain_ci95"],
         "class": stats[best]["class"],
+        "gemm_bound": stats[best]["gemm_bound"],
+        # the strict T_comm's engine decides the collective's bound
+        "coll_bound": coll_bound_strict(per_mode, modes, plateaus, w.coll_bytes),
+        "settle_us": settle_us, "coll_plateau_gbs": {k: v / 1e9 for k, v in plateaus.items()},
         "gemm_tflops_overlap": stats[best]["gemm_tflops_overlap"],
         "copy_gbs_overlap": stats[best]["copy_gbs_overlap"],
         "roofline": roof, "roofline_copy": copy_roof,
@@ -963,7 +1045,8 @@ def main(argv=None):
         if rank == 0:
             emit_detail({"detail": "aux", **detail["aux"]}, args.detail_out)
     if not args.no_e2e:
-        detail["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args)
+        detail["e2e"] = e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args,
+                                    settle_us)
         if rank == 0:
             emit_detail({"detail": "e2e", **detail["e2e"]}, args.detail_out)
     if not args.no_cpu_baseline and world == 1 and rank == 0:
@@ -1022,7 +1105,7 @@ def headline_line(d):
         "config": {"workload": cfg["workload"], "M": cfg["M"], "N": cfg["N"], "K": cfg["K"],
                    "collective": cfg["collective"], "coll_src": cfg["coll_src"],
                    "l2": "flushed before every timed phase (2 x L2 zero-fill)",
-                   "parallelism": cfg["parallelism"]},
+                   "settle_us": d.get("settle_us"), "parallelism": cfg["parallelism"]},
         "best_mode": d["best_mode"], "value_ci95": d.get("value_ci95"),
         "modes_pct": {k: v["pct_ideal_gain"] for k, v in d.get("modes", {}).items()},
         "class": d.get("class"),
@@ -1070,6 +1153,34 @@ def _event_time(torch, stream, fn, reps, warm, flush=None):
         e1.synchronize()
         ts.append(e0.elapsed_time(e1) * 1e-3)
     return statistics.fmean(ts), ts
+
+
+def measure_plateaus(c3, torch, w, dev, stream, flush):
+    """Plateau rate (output bytes/s) of the workload's collective kind on each
+    engine: the best isolated rate over totals of 256 MiB, 512 MiB and 1 GiB
+    (the top of the pages' 1 MiB - 1 GiB sweep, where the rate has levelled
+    off).  The all-reduce's plateau is that of its all-gather.  Device-resident
+    buffers, L2 flushed before each run."""
+    kind = "alltoall" if w.coll == "alltoall" else "allgather"
+    cid = c3.C3_COLL_ALLTOALL if kind == "alltoall" else c3.C3_COLL_ALLGATHER
+    best = {"sm": 0.0, "ce": 0.0}
+    for total in (256 << 20, 512 << 20, 1 << 30):
+        src = torch.empty(total, dtype=torch.uint8, device=dev)
+        dst = torch.empty(total, dtype=torch.uint8, device=dev)
+        if kind == "alltoall":
+            prob = c3.Problem(None, None, None, 0, 0, 0, cid, dst, total // 64, 8, send=src, stream=stream)
+        else:
+            unit = total // 8
+            shards = [src[i * unit:(i + 1) * unit] for i in range(8)]
+            prob = c3.Problem(None, None, None, 0, 0, 0, cid, dst, unit, 8, shards=shards, stream=stream)
+        for eng, mode in (("sm", c3.C3_MODE_SERIAL_SM), ("ce", c3.C3_MODE_SERIAL_CE)):
+            ts = []
+            for _ in range(4):
+                c3.c3_l2_flush(flush, flush.numel(), stream)
+                ts.append(c3.c3_run(prob, mode, 0, 0)["t_conc"])
+            best[eng] = max(best[eng], total / statistics.median(ts[1:]))
+        del src, dst, prob
+    return best
 
 
 def aux_measure(c3, torch, w, dev, stream, peaks, dshards, dsend, out, info):
@@ -1122,7 +1233,7 @@ def aux_measure(c3, torch, w, dev, stream, peaks, dshards, dsend, out, info):
     return res
 
 
-def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args):
+def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, stream, args, settle_us=0):
     """The same metric end to end through the public API with the step's
     inputs in pinned host memory.  The GEMM chain copies A in, runs c3_gemm
     and reads C back; the collective reads its sources straight from the
@@ -1170,6 +1281,8 @@ def e2e_measure(c3, torch, np, w, A_h, payload, dA, dB, dshards, dC, out, dev, s
     def timed(fn):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
+        if settle_us:
+            time.sleep(settle_us * 1e-6)  # the same idle period the device-side timer takes
         e0.record(stream)
         fn(e0)
         e1.record(stream)

@@ -41,14 +41,20 @@ class C3Problem(ctypes.Structure):
                 ("coll", _int), ("shards", ctypes.POINTER(_vp)), ("send", _vp), ("recv", _vp),
                 ("unit_bytes", _sz), ("nranks", _int), ("comm_sms", _int), ("sm_kernel", _int), ("coll_l2", _int),
                 ("ce_variant", _int),
-                ("flush_buf", _vp), ("flush_bytes", _sz), ("stream", _vp)]
+                ("flush_buf", _vp), ("flush_bytes", _sz), ("stream", _vp),
+                ("settle_us", _int), ("peak_flops", ctypes.c_double), ("peak_bytes_per_s", ctypes.c_double),
+                ("coll_plateau_sm", ctypes.c_double), ("coll_plateau_ce", ctypes.c_double)]
 
 
 _TIMING_DOUBLES = ["t_gemm_iso", "t_comm_iso", "t_serial", "t_serial_meas", "t_conc", "t_ideal", "s_ideal",
                    "s_real", "pct_ideal_gain", "pct_ideal_ratio", "t_gemm_dev", "t_comm_dev", "t_gemm_ev",
                    "t_comm_ev"]
 _TIMING_INTS = ["cls", "mode", "sm_split", "priority", "gemm_ctas", "comm_ctas", "gemm_sms", "comm_sms",
-                "smid_overlap", "sms_shared_any", "status"]
+                "smid_overlap", "sms_shared_any", "status", "gemm_bound", "coll_bound"]
+C3_BOUND_UNKNOWN, C3_GEMM_COMPUTE, C3_GEMM_MEMORY = -1, 0, 1
+C3_COLL_LATENCY, C3_COLL_BANDWIDTH = 0, 1
+GEMM_BOUND_NAMES = {-1: "unknown", 0: "compute", 1: "memory"}
+COLL_BOUND_NAMES = {-1: "unknown", 0: "latency", 1: "bandwidth"}
 
 
 class C3Timing(ctypes.Structure):
@@ -57,6 +63,8 @@ class C3Timing(ctypes.Structure):
     def as_dict(self):
         d = {n: getattr(self, n) for n in _TIMING_DOUBLES + _TIMING_INTS}
         d["class"] = CLASS_NAMES.get(self.cls, "?")
+        d["gemm_bound_name"] = GEMM_BOUND_NAMES.get(self.gemm_bound, "?")
+        d["coll_bound_name"] = COLL_BOUND_NAMES.get(self.coll_bound, "?")
         return d
 
 
@@ -257,7 +265,8 @@ class Problem:
 
     def __init__(self, A, B, C, M, N, K, coll, recv, unit_bytes, nranks=8, shards=None, send=None,
                  comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None, coll_l2=C3_L2_NORMAL,
-                 ce_variant=C3_CE_PER_SEGMENT):
+                 ce_variant=C3_CE_PER_SEGMENT, settle_us=0, peak_flops=0.0, peak_bytes_per_s=0.0,
+                 coll_plateau_sm=0.0, coll_plateau_ce=0.0):
         self._shard_arr = None
         if shards is not None:
             self._shard_arr = (_vp * len(shards))(*[_ptr(s) for s in shards])
@@ -265,7 +274,8 @@ class Problem:
         self.rec = C3Problem(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(coll),
                              self._shard_arr, _ptr(send), _ptr(recv), int(unit_bytes), int(nranks),
                              int(comm_sms), int(sm_kernel), int(coll_l2), int(ce_variant), fb, fn,
-                             _stream(stream))
+                             _stream(stream), int(settle_us), float(peak_flops), float(peak_bytes_per_s),
+                             float(coll_plateau_sm), float(coll_plateau_ce))
 
 
 def c3_run(problem: Problem, mode, sm_split=0, priority=0, check=True):

@@ -432,6 +432,10 @@ static int check_problem(const c3_problem* p, CollPlan* cp) {
     if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH_PARALLEL)
         return set_error(C3_EINVAL, "bad ce_variant");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
+    if (p->settle_us < 0 || p->settle_us > 1000000) return set_error(C3_EINVAL, "settle_us must be 0 .. 1000000");
+    // each rate: 0 (unknown) or a positive finite number (NaN fails every comparison)
+    for (double v : {p->peak_flops, p->peak_bytes_per_s, p->coll_plateau_sm, p->coll_plateau_ce})
+        if (!(v >= 0.0 && v <= 1e300)) return set_error(C3_EINVAL, "peaks and plateaus must be >= 0 and finite");
     if (p->flush_buf && !aligned16(p->flush_buf)) return set_error(C3_EALIGN, "flush_buf must be 16-byte aligned");
     const size_t cb = p->coll == C3_COLL_ALLREDUCE ? p->unit_bytes * (size_t)p->nranks
                                                    : t->seg_bytes * (size_t)t->nseg;
@@ -543,10 +547,19 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     return read_status(ds, out);
 }
 
+// The settle period before a timed phase (c3_problem.settle_us): the previous
+// phase has completed (every phase ends with a host wait on its last event),
+// so the GPU idles for this long and each phase starts from the same clock
+// and power state.
+static void settle(const c3_problem* p) {
+    if (p->settle_us > 0) std::this_thread::sleep_for(std::chrono::microseconds(p->settle_us));
+}
+
 // Times one phase that runs entirely on `s0`: fn() enqueues it.
 template <class F>
 static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, const char* name, double* t_out, F fn) {
     PhaseRange range(name);
+    settle(p);
     int rc;
     if (p->flush_buf && p->flush_bytes && (rc = l2_flush_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
     cudaError_t e;
@@ -556,6 +569,29 @@ static int time_phase(DeviceState& ds, cudaStream_t s0, const c3_problem* p, con
     if ((rc = wait_event(ds.ev[5], 120.0))) return rc;
     *t_out = elapsed_s(ds.ev[4], ds.ev[5]);
     return C3_OK;
+}
+
+// Output bytes of the problem's collective (what its rate is counted in).
+static double coll_out_bytes(const c3_problem* p, const CollPlan& t) {
+    if (p->coll == C3_COLL_ALLREDUCE) return (double)p->unit_bytes * (double)p->nranks;
+    return (double)t.seg.seg_bytes * (double)t.seg.nseg;
+}
+
+// The taxonomy's other two axes (c3_gemm_bound, c3_coll_bound in c3_api.h):
+// the GEMM against the roofline ridge, the collective's isolated rate against
+// half the plateau of its engine's size sweep.  Both compared cross-multiplied.
+static void fill_bounds(c3_timing* r, const c3_problem* p, const CollPlan& t, int engine) {
+    const double M = (double)p->M, N = (double)p->N, K = (double)p->K;
+    const double flops = 2.0 * M * N * K;
+    const double bytes = 2.0 * M * K + 2.0 * N * K + 4.0 * M * N;
+    r->gemm_bound = C3_BOUND_UNKNOWN;
+    if (p->peak_flops > 0.0 && p->peak_bytes_per_s > 0.0 && flops > 0.0 && bytes > 0.0)
+        r->gemm_bound = (flops * p->peak_bytes_per_s < bytes * p->peak_flops) ? C3_GEMM_MEMORY : C3_GEMM_COMPUTE;
+    const double plateau = engine == C3_ENGINE_CE ? p->coll_plateau_ce : p->coll_plateau_sm;
+    const double cb = coll_out_bytes(p, t);
+    r->coll_bound = C3_BOUND_UNKNOWN;
+    if (plateau > 0.0 && cb > 0.0 && r->t_comm_iso > 0.0)
+        r->coll_bound = (2.0 * cb >= plateau * r->t_comm_iso) ? C3_COLL_BANDWIDTH : C3_COLL_LATENCY;
 }
 
 static void fill_metrics(c3_timing* r) {
@@ -771,6 +807,11 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only");
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
+    if (p->settle_us > 0) {
+        // the first settle period must start from an idle stream too
+        cudaError_t e = cudaStreamSynchronize(s0);
+        if (e != cudaSuccess) return set_cuda_error(e, "stream synchronize");
+    }
     for (int it = 0; it < warmup + reps; ++it) {
         c3_timing r;
         std::memset(&r, 0, sizeof r);
@@ -788,6 +829,7 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
             return r1 ? r1 : launch_coll(*ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, p->comm_sms, false, s0, nullptr);
         });
         if (rc) return rc;
+        settle(p);
         if (p->flush_buf && p->flush_bytes && (rc = l2_flush_launch(p->flush_buf, p->flush_bytes, s0))) return rc;
         r.mode = mode;
         r.sm_split = sm_split;
@@ -796,6 +838,7 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
         r.status = rc;
         if (rc) return rc;
         fill_metrics(&r);
+        fill_bounds(&r, p, t, engine);
         if (it >= warmup) per_rep[it - warmup] = r;
     }
     return C3_OK;

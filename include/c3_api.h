@@ -119,6 +119,21 @@ typedef enum {
 /* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
 typedef enum { C3_CLASS_G_LONG = 0, C3_CLASS_GC_EQUAL = 1, C3_CLASS_C_LONG = 2 } c3_class;
 
+/* The taxonomy's other two axes (the pith.science verdict's summary of the
+ * paper's taxonomy: compute- versus memory-bound GEMMs, latency- versus
+ * bandwidth-bound collectives; Section III).
+ *   GEMM: memory-bound when its arithmetic intensity 2MNK / (2MK + 2NK + 4MN)
+ *     lies below the roofline ridge peak_flops / peak_bytes_per_s (compared
+ *     cross-multiplied), compute-bound otherwise.
+ *   Collective: bandwidth-bound when its isolated rate (output bytes /
+ *     t_comm_iso) reaches half the plateau rate of the same engine's size
+ *     sweep, latency-bound below -- the plateau threshold the referee's minor
+ *     comment on Section III asks for in place of "latency does not grow with
+ *     size".
+ * UNKNOWN when the problem carries no peaks / no plateau for that engine. */
+typedef enum { C3_BOUND_UNKNOWN = -1, C3_GEMM_COMPUTE = 0, C3_GEMM_MEMORY = 1 } c3_gemm_bound;
+typedef enum { C3_COLL_LATENCY = 0, C3_COLL_BANDWIDTH = 1 } c3_coll_bound;
+
 typedef struct {
     int device;           /* CUDA ordinal */
     int sm_count;         /* streaming multiprocessors */
@@ -254,6 +269,20 @@ typedef struct {
     void *flush_buf;
     size_t flush_bytes;
     c3_stream stream;          /* runs fork from and join back to this stream */
+    /* Timer options (c3_time).  Zero leaves each one off. */
+    int settle_us;             /* idle time before each timed phase: the host sleeps this long after
+                                  the previous phase completed (0..1000000 us).  A GB300 at its power
+                                  limit runs a phase that follows an idle period at higher clocks than
+                                  one that follows seconds of load, so without a common idle period
+                                  the isolated and concurrent phases are timed in different power
+                                  states. */
+    double peak_flops;         /* dense bf16 tensor peak, FLOP/s: with peak_bytes_per_s, classifies
+                                  the GEMM as compute- or memory-bound (0 = unknown) */
+    double peak_bytes_per_s;   /* memory bandwidth peak, bytes/s (0 = unknown) */
+    double coll_plateau_sm;    /* plateau rate of the SM collective over a size sweep, output bytes
+                                  per second: classifies the collective as latency- or
+                                  bandwidth-bound (0 = unknown) */
+    double coll_plateau_ce;    /* the same for the copy-engine (memcpy) collective */
 } c3_problem;
 
 /* Times in seconds. */
@@ -283,6 +312,8 @@ typedef struct {
                               same time, by their %globaltimer windows (0 = the partition held) */
     int sms_shared_any;    /* SMs that ran CTAs of both kernels at any time during the run */
     int status;            /* C3_OK or the run's device status */
+    int gemm_bound;        /* c3_gemm_bound of the problem's GEMM                     (c3_time) */
+    int coll_bound;        /* c3_coll_bound of t_comm_iso on the mode's engine          (c3_time) */
 } c3_timing;
 
 /*
@@ -325,9 +356,12 @@ int c3_run(const c3_problem *p, int mode, int sm_split, int priority, c3_timing 
  * The C3 timer: `warmup` untimed repetitions, then `reps` timed repetitions,
  * each made of: GEMM alone (every SM), collective alone (the mode's engine,
  * default budget), serial (GEMM then collective), and the requested mode.
- * When p->flush_buf is set, L2 is flushed before each phase.  per_rep[r] (reps
+ * When p->settle_us is set, the host waits that long before each phase (after
+ * synchronising p->stream once at entry); when p->flush_buf is set, L2 is then
+ * flushed before each phase, outside its timed interval.  per_rep[r] (reps
  * entries, host memory) receives every field, with the speedups of repetition
- * r computed from that repetition's own isolated times.
+ * r computed from that repetition's own isolated times, and the taxonomy
+ * class and bounds of the pair.
  */
 int c3_time(const c3_problem *p, int mode, int sm_split, int priority, int warmup, int reps,
             c3_timing *per_rep);

@@ -46,7 +46,9 @@ int main(void) {
   printf("c3_problem %zu\nc3_timing %zu\nc3_device_info %zu\n", sizeof(c3_problem), sizeof(c3_timing), sizeof(c3_device_info));
   F(c3_problem, coll); F(c3_problem, shards); F(c3_problem, unit_bytes); F(c3_problem, nranks);
   F(c3_problem, sm_kernel); F(c3_problem, flush_buf); F(c3_problem, stream);
+  F(c3_problem, settle_us); F(c3_problem, peak_flops); F(c3_problem, coll_plateau_ce);
   F(c3_timing, t_comm_ev); F(c3_timing, cls); F(c3_timing, smid_overlap); F(c3_timing, status);
+  F(c3_timing, gemm_bound); F(c3_timing, coll_bound);
   F(c3_device_info, comm_default_sms);
   return 0;
 }
@@ -129,6 +131,13 @@ def test_run_and_time_reject_bad_records(c3):
     overlap = c3.Problem(0x1000, 0x2000, 0x100000, 4, 4, 16, c3.C3_COLL_ALLGATHER, 0x100000, 32,
                          shards=[0x10000 * (r + 1) for r in range(8)])
     assert c3.lib().c3_run(ctypes.byref(overlap.rec), 1, 0, 0, ctypes.byref(t)) == c3.C3_EINVAL
+    # timer options: settle period and the rates of the taxonomy's bounds
+    for kw in ({"settle_us": -1}, {"settle_us": 1000001}, {"peak_flops": -1.0}, {"peak_bytes_per_s": float("nan")},
+               {"coll_plateau_sm": float("inf")}, {"coll_plateau_ce": -2.0}):
+        q = c3.Problem(0x1000, 0x2000, 0x3000, 4, 4, 16, c3.C3_COLL_ALLGATHER, 0x100000, 32,
+                       shards=[0x10000 * (r + 1) for r in range(8)], **kw)
+        assert c3.lib().c3_time(ctypes.byref(q.rec), 1, 0, 0, 0, 1, arr) == c3.C3_EINVAL, kw
+        assert c3.lib().c3_run(ctypes.byref(q.rec), 1, 0, 0, ctypes.byref(t)) == c3.C3_EINVAL, kw
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -206,3 +206,34 @@ def test_gemm_rows_reference_in_chunks_equals_one_pass():
     ref2, b2 = bench.gemm_rows_reference(np, A, B, rows, chunk=97)      # ragged last chunk
     # the same fp64 dot products; a BLAS may block K differently per shape, so allow its last bits
     assert np.allclose(ref1, ref2, rtol=1e-12, atol=1e-12) and np.allclose(b1, b2, rtol=1e-12, atol=0)
+
+
+def test_settle_period_follows_the_gemm_time_within_its_clamp():
+    assert bench.auto_settle_us(7.4e-3) == 18500           # 2.5 x 7.4 ms
+    assert bench.auto_settle_us(1.0) == 20000              # clamped to 20 ms
+    assert bench.auto_settle_us(10e-6) == 200              # clamped to 0.2 ms
+    assert bench.auto_settle_us(7.4e-3, settle_ms=0) == 0  # explicit values win
+    assert bench.auto_settle_us(7.4e-3, settle_ms=3.5) == 3500
+
+
+def test_pooled_gemm_time_is_the_per_step_mean_over_modes():
+    per_mode = {"a": [{"t_gemm_iso": 1.0}, {"t_gemm_iso": 3.0}],
+                "b": [{"t_gemm_iso": 2.0}, {"t_gemm_iso": 5.0}, {"t_gemm_iso": 9.0}]}
+    assert bench.pooled_gemm_times(per_mode) == [1.5, 4.0]   # steps both modes completed
+
+
+def test_share_ci_uses_the_pooled_gemm_times_when_given():
+    recs = _recs([100.0] * 10, [120.0] * 10)
+    lo, hi = bench.share_ci95(recs, 40.0, tg_steps=[110.0] * 10)
+    point = bench.pct_gain(110.0, 40.0, 120.0)["pct_ideal_gain"]
+    assert lo == pytest.approx(point) and hi == pytest.approx(point)
+
+
+def test_collective_bound_of_the_strict_engine():
+    modes = [("baseline", 1, 0, 0), ("ce", 2, 0, 0)]
+    per_mode = {"baseline": [{"t_comm_iso": 2.0}], "ce": [{"t_comm_iso": 4.0}]}
+    # SM engine is faster (2 s for 1 byte = 0.5 B/s); against its plateau of 1 B/s that is exactly half
+    assert bench.coll_bound_strict(per_mode, modes, {"sm": 1.0, "ce": 100.0}, 1) == "bandwidth"
+    assert bench.coll_bound_strict(per_mode, modes, {"sm": 1.01, "ce": 0.1}, 1) == "latency"
+    assert bench.coll_bound_strict(per_mode, modes, {}, 1) == "unknown"
+    assert bench.most_common(["a", "b", "b"]) == "b" and bench.most_common([]) is None

@@ -159,3 +159,32 @@ def test_every_mode_under_c3_time_stays_exact(c3, setup):
         setup.poison()
         c3.c3_time(setup.p, mode, split, prio, warmup=0, reps=2)
         setup.verify()
+
+
+@pytest.mark.parametrize("plateau_scale", [0.25, 4.0])
+def test_timer_bounds_and_settle_follow_their_definitions(c3, setup, plateau_scale):
+    """c3_time's gemm_bound / coll_bound equal the oracle's classification of
+    the same times and rates, on both sides of the collective's threshold,
+    and a settle period leaves the outputs exact and the timer's fields
+    consistent."""
+    w = setup.w
+    first = c3.c3_time(setup.p, 1, 0, 0, warmup=0, reps=1)[0]
+    # a plateau that puts this collective clearly on one side of half-plateau
+    rate = w.coll_bytes / first["t_comm_iso"]
+    plateau = rate * plateau_scale
+    peak_flops, peak_bw = 1.9e15, 6.8e12
+    p = c3.Problem(setup.dA, setup.dB, setup.dC, w.M, w.N, w.K, setup.p.rec.coll, setup.out, w.unit_bytes,
+                   w.nranks, shards=setup.dshards, send=setup.dsend, flush=setup.flush, settle_us=300,
+                   peak_flops=peak_flops, peak_bytes_per_s=peak_bw, coll_plateau_sm=plateau, coll_plateau_ce=plateau)
+    setup.poison()
+    for mode in (1, 2):
+        for r in c3.c3_time(p, mode, 0, 0, warmup=0, reps=3):
+            g, c = oracle.c3_bounds(w.gemm_flops, w.gemm_bytes, peak_flops, peak_bw, w.coll_bytes,
+                                    r["t_comm_iso"], plateau)
+            assert r["gemm_bound_name"] == g and r["coll_bound_name"] == c
+            m = oracle.c3_metrics(r["t_gemm_iso"], r["t_comm_iso"], r["t_conc"])
+            assert r["s_ideal"] == pytest.approx(m["s_ideal"], rel=1e-12)
+    setup.verify()
+    # no peaks, no plateau: both axes unknown
+    r = c3.c3_time(setup.p, 1, 0, 0, warmup=0, reps=1)[0]
+    assert r["gemm_bound"] == c3.C3_BOUND_UNKNOWN and r["coll_bound"] == c3.C3_BOUND_UNKNOWN
