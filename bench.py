@@ -63,8 +63,10 @@ MODES = [
     ("partitioned_32", 1, 32, 0),
     ("partitioned_64", 1, 64, 0),
     ("prio_partitioned_32", 1, 32, 1),
+    ("reclaim_8", 4, 8, 0),
     ("reclaim_16", 4, 16, 0),
     ("reclaim_32", 4, 32, 0),
+    ("reclaim_64", 4, 64, 0),
     ("ce", 2, 0, 0),
     ("ce_rp_8", 2, 8, 0),
     ("ce_rp_16", 2, 16, 0),
@@ -73,10 +75,11 @@ MODES = [
 # Modes a workload runs by default (every mode otherwise).  The Llama-405B
 # pair names its own set: the copy kernel on every SM, on 8/16/32 SMs, and
 # the copy-engine path with and without SMs taken from the GEMM; the
-# prioritised launch and the partition with reclaim ride along.
+# prioritised launch and the partitions with reclaim (the GEMM takes the
+# collective's SMs back once it is done) ride along.
 DEFAULT_MODES = {
-    "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_16",
-                 "ce", "ce_rp_8"],
+    "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_8",
+                 "reclaim_16", "reclaim_32", "reclaim_64", "ce", "ce_rp_8"],
 }
 
 

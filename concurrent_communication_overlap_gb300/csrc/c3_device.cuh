@@ -44,9 +44,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Stamp the start of a CTA: min start time, the SM bitmap and this CTA's
-// residency record.
-__device__ __forceinline__ void stamp_begin(DevStatus* st, bool is_gemm) {
+// Stamp the start of a CTA: min start time, the SM bitmap and the residency
+// record `idx` (the CTA's index within its launch group; blockIdx.x unless
+// the kernel is one of several launches sharing one group).
+__device__ __forceinline__ void stamp_begin(DevStatus* st, bool is_gemm, unsigned idx) {
     if (st == nullptr) return;
     unsigned long long t = globaltimer();
     uint32_t sm = smid();
@@ -54,25 +55,45 @@ __device__ __forceinline__ void stamp_begin(DevStatus* st, bool is_gemm) {
     if (is_gemm) {
         atomicMin(&st->gemm_t0, t);
         atomicOr(&st->smid_gemm[(sm >> 5) & 7], 1u << (sm & 31));
-        if (blockIdx.x < (unsigned)kCtaRecs) rec = &st->gemm_rec[blockIdx.x];
+        if (idx < (unsigned)kCtaRecs) rec = &st->gemm_rec[idx];
     } else {
         atomicMin(&st->comm_t0, t);
         atomicOr(&st->smid_comm[(sm >> 5) & 7], 1u << (sm & 31));
-        if (blockIdx.x < (unsigned)kCtaRecs) rec = &st->comm_rec[blockIdx.x];
+        if (idx < (unsigned)kCtaRecs) rec = &st->comm_rec[idx];
     }
     if (rec) {
         rec->smid = sm;
         rec->t0 = t;
     }
 }
+__device__ __forceinline__ void stamp_begin(DevStatus* st, bool is_gemm) { stamp_begin(st, is_gemm, blockIdx.x); }
 
-__device__ __forceinline__ void stamp_end(DevStatus* st, bool is_gemm) {
+__device__ __forceinline__ void stamp_end(DevStatus* st, bool is_gemm, unsigned idx) {
     if (st == nullptr) return;
     unsigned long long t = globaltimer();
     atomicMax(is_gemm ? &st->gemm_t1 : &st->comm_t1, t);
-    if (blockIdx.x < (unsigned)kCtaRecs) {
-        CtaRec* rec = is_gemm ? &st->gemm_rec[blockIdx.x] : &st->comm_rec[blockIdx.x];
+    if (idx < (unsigned)kCtaRecs) {
+        CtaRec* rec = is_gemm ? &st->gemm_rec[idx] : &st->comm_rec[idx];
         rec->t1 = t;
+        rec->used = 1;
+    }
+}
+__device__ __forceinline__ void stamp_end(DevStatus* st, bool is_gemm) { stamp_end(st, is_gemm, blockIdx.x); }
+
+// Both stamps at once, for a CTA that records its window only at the end
+// (once it knows it did any work): start t0, end t1.
+__device__ __forceinline__ void stamp_window(DevStatus* st, bool is_gemm, unsigned idx, unsigned long long t0,
+                                             unsigned long long t1) {
+    if (st == nullptr) return;
+    uint32_t sm = smid();
+    atomicMin(is_gemm ? &st->gemm_t0 : &st->comm_t0, t0);
+    atomicMax(is_gemm ? &st->gemm_t1 : &st->comm_t1, t1);
+    atomicOr(is_gemm ? &st->smid_gemm[(sm >> 5) & 7] : &st->smid_comm[(sm >> 5) & 7], 1u << (sm & 31));
+    if (idx < (unsigned)kCtaRecs) {
+        CtaRec* rec = is_gemm ? &st->gemm_rec[idx] : &st->comm_rec[idx];
+        rec->smid = sm;
+        rec->t0 = t0;
+        rec->t1 = t1;
         rec->used = 1;
     }
 }

@@ -38,6 +38,12 @@ struct DevStatus {
     // the per-run reset leaves them alone (a GEMM of another stream may be
     // using a slot).
     unsigned int sched[kSchedSlots][2];
+    // Work counters of the SM copy kernels, the same way: per slot, the next
+    // work unit (a 64 KiB round or a 32 KiB chunk) and the number of CTAs
+    // done.  One slot serves a launch group -- one launch, or several on
+    // different streams that share the collective's work -- and its last CTA
+    // puts the slot back to zero.
+    unsigned int coll_sched[kSchedSlots][2];
 };
 
 constexpr size_t kStatusBytes = 16384;
@@ -98,6 +104,8 @@ struct DeviceState {
     cudaEvent_t ev[8] = {};
     DevStatus* status = nullptr;       // device status block
     unsigned int next_sched = 0;       // round-robin scheduler slot
+    unsigned int next_coll_sched = 0;  // round-robin copy work-counter slot
+    cudaStream_t s_comm_b = nullptr;   // second collective stream: the CTAs that wait for the GEMM's SMs
     bool ready = false;
 };
 
@@ -137,8 +145,19 @@ int gemm_describe(int64_t M, int64_t N, int64_t K, int cap, int* bn, int* msub, 
 int gemm_smem_bytes();  // dynamic shared memory of the largest GEMM tile configuration
 int gemm_init_device();  // function attributes; once per device
 
-int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, int l2_stream, cudaStream_t s,
-                   DevStatus* st, int* ctas_out);
+// A group of SM copy launches sharing one work counter: `total_ctas` CTAs over
+// every launch of the group; each launch numbers its CTAs from `cta_base`.
+struct CopyGroup {
+    unsigned int* work = nullptr;  // DevStatus::coll_sched slot
+    int total_ctas = 0;
+};
+// Picks the next work-counter slot of the device (round robin).
+CopyGroup copy_group(DeviceState& ds, int total_ctas);
+int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out);
+// Largest number of work units (64 KiB rounds / 32 KiB chunks) a collective may
+// have: the 32-bit counters stay far from wrapping.
+bool copy_units_fit(const SegTable& t);
 int copy_init_device(int max_reserve);
 int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStream_t s, DevStatus* st,
                           int* ctas_out);

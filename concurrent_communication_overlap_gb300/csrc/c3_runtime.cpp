@@ -82,6 +82,7 @@ static int init_device(DeviceState& ds, int dev) {
     C3_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi), "stream priority range");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
+    C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_b, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithFlags(&ds.s_capture, cudaStreamNonBlocking), "stream");
     for (auto& ev : ds.ev) C3_TRY(cudaEventCreate(&ev), "event");
     if (take_fault(kFaultDeviceInit))
@@ -100,6 +101,7 @@ static int init_device(DeviceState& ds, int dev) {
 static void release_device(DeviceState& ds) {
     if (ds.s_comm) cudaStreamDestroy(ds.s_comm);
     if (ds.s_comm_hi) cudaStreamDestroy(ds.s_comm_hi);
+    if (ds.s_comm_b) cudaStreamDestroy(ds.s_comm_b);
     if (ds.s_capture) cudaStreamDestroy(ds.s_capture);
     if (ds.device >= 0) ce_release_graphs(ds.device);
     for (auto& ev : ds.ev)
@@ -313,37 +315,79 @@ static int locate_plan(const DeviceState& ds, CollPlan* cp) {
     return C3_OK;
 }
 
-// One collective launch.  SM engine: `budget` CTAs (0 = default); exclusive =
-// the CTAs keep their SMs to themselves (partitioning).
+// The SM copy kernel a collective runs on, and the shared memory its CTAs
+// reserve: exclusive CTAs (partitioning) keep their SMs to themselves.
+static int pick_flavour(const SegTable& t, int sm_kernel, bool exclusive) {
+    return sm_kernel == C3_SMK_VEC ? kSmkVec
+           : sm_kernel == C3_SMK_BULK ? kSmkBulk
+           : (exclusive && !t.host_src ? kSmkBulk : kSmkVec);
+}
+
+// One collective launch.  SM engine: `budget` CTAs (0 = default), one launch
+// group; exclusive = the CTAs keep their SMs to themselves (partitioning).
+// With `split_total` > budget the collective is the first part of a split
+// group of split_total CTAs (launch_coll_rest launches the others); the
+// reduce-scatter of an all-reduce then records ds.ev[7], which the rest waits
+// for.  *group receives the group (SM engine).
 static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_kernel, int l2_stream, int ce_variant,
-                       int budget, bool exclusive, cudaStream_t s, int* ctas) {
+                       int budget, bool exclusive, cudaStream_t s, int* ctas, int split_total = 0,
+                       CopyGroup* group = nullptr) {
     if (ctas) *ctas = 0;
     const SegTable& t = cp.seg;
-    if (cp.has_rs) {
-        // the reduce-scatter needs arithmetic: always SMs, whatever the engine
-        int k = budget > 0 ? budget : default_comm_sms(ds);
-        if (k > ds.sm_count) k = ds.sm_count;
-        int rc = reduce_scatter_launch(cp.rs, k, exclusive ? exclusive_reserve(ds) : 0, s, ds.status, ctas);
-        if (rc) return rc;
-        if (t.nseg == 0) return 0;
-        int dummy = 0;
-        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
-        int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
-                      : sm_kernel == C3_SMK_BULK ? kSmkBulk
-                      : (exclusive ? kSmkBulk : kSmkVec);
-        int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-        return copy_sm_launch(t, k, flavour, reserve, l2_stream, s, ds.status, &dummy);
-    }
-    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
     int k = budget > 0 ? budget : default_comm_sms(ds);
     if (k > ds.sm_count) k = ds.sm_count;
-    if (t.host_src && sm_kernel == C3_SMK_BULK)
+    const int total = split_total > k ? split_total : k;
+    if (engine == C3_ENGINE_SM && t.host_src && sm_kernel == C3_SMK_BULK)
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only; host sources take the vector kernel");
-    int flavour = sm_kernel == C3_SMK_VEC ? kSmkVec
-                  : sm_kernel == C3_SMK_BULK ? kSmkBulk
-                  : (exclusive && !t.host_src ? kSmkBulk : kSmkVec);
-    int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-    return copy_sm_launch(t, k, flavour, reserve, l2_stream, s, ds.status, ctas);
+    if (cp.has_rs) {
+        // the reduce-scatter needs arithmetic: always SMs, whatever the engine
+        int rc = reduce_scatter_launch(cp.rs, k, exclusive ? exclusive_reserve(ds) : 0, s, ds.status, ctas);
+        if (rc) return rc;
+        if (split_total > k) {
+            cudaError_t e = cudaEventRecord(ds.ev[7], s);
+            if (e != cudaSuccess) return set_cuda_error(e, "event record");
+        }
+        if (t.nseg == 0) return 0;
+        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
+        const int flavour = pick_flavour(t, sm_kernel, exclusive);
+        const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
+        CopyGroup g = copy_group(ds, total);
+        if (group) *group = g;
+        int dummy = 0;
+        return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, &dummy);
+    }
+    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
+    const int flavour = pick_flavour(t, sm_kernel, exclusive);
+    const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
+    CopyGroup g = copy_group(ds, total);
+    if (group) *group = g;
+    return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, ctas);
+}
+
+// The rest of a split SM collective: `rest` more CTAs of group `g`, numbered
+// from `first`, exclusive like the first part, on stream `s2`.  Launched after
+// the GEMM, so its CTAs start only on SMs the GEMM has left: the collective
+// widens to them once the GEMM's CTAs finish (a CTA that finds no work left
+// exits at once).  An all-reduce's copies wait for its reduce-scatter.
+static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, int l2_stream, int first, int rest,
+                            const CopyGroup& g, cudaStream_t s2, int* ctas) {
+    if (ctas) *ctas = 0;
+    const SegTable& t = cp.seg;
+    if (rest <= 0 || t.nseg == 0 || t.seg_bytes == 0) return 0;
+    if (cp.has_rs) {
+        cudaError_t e = cudaStreamWaitEvent(s2, ds.ev[7], 0);
+        if (e != cudaSuccess) return set_cuda_error(e, "wait for the reduce-scatter");
+    }
+    const int flavour = pick_flavour(t, sm_kernel, true);
+    const int reserve = flavour == kSmkVec ? exclusive_reserve(ds) : 0;
+    return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas);
+}
+
+// A split group whose second part could not be launched would never count to
+// its total, so its work counter would stay dirty: clear it behind the first
+// part, on the first part's stream.
+static void abandon_group(const CopyGroup& g, cudaStream_t s) {
+    if (g.work) cudaMemsetAsync(g.work, 0, 2 * sizeof(unsigned int), s);
 }
 
 static int wait_event(cudaEvent_t ev, double limit_s) {
@@ -402,8 +446,9 @@ static int read_status(DeviceState& ds, c3_timing* out) {
         out->smid_overlap = coresident_sms(h, &out->sms_shared_any);
     }
     if (h.error) {
-        // a launch that gave up may have left its tile-scheduler slot non-zero
+        // a launch that gave up may have left its tile-scheduler or copy work slot non-zero
         gemm_sched_reset(ds.status);
+        cudaMemset(ds.status->coll_sched, 0, sizeof ds.status->coll_sched);
         char buf[128];
         std::snprintf(buf, sizeof buf, "device wait gave up (site %d)", h.where);
         return set_error(h.error, buf);
@@ -476,6 +521,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     if (rc) return rc;
     cudaError_t e;
     int gctas = 0, cctas = 0;
+    bool split_rest = false;  // the collective ran as a split launch group (second part on ds.ev[6])
     const bool serial = (mode == C3_MODE_SERIAL_SM || mode == C3_MODE_SERIAL_CE);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
     // Host-side GEMM planning (tile choice, tensor maps) happens before the
@@ -505,39 +551,79 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         const bool reclaim = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
         if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
-        // reclaim: the GEMM is launched on every SM and its CTAs that find no
-        // free SM start when the collective's SMs free up
+        // Partitioning (sm_split > 0 on SMs): the collective starts on sm_split
+        // SMs it holds alone and the GEMM on the others (capped at SM count -
+        // sm_split, or, with reclaim, launched on every SM so that its CTAs
+        // that find no free SM start as the collective's SMs free up).  The
+        // collective is one launch group of SM-count CTAs in two parts: the
+        // first sm_split CTAs, and the rest launched after the GEMM on a
+        // second stream, whose CTAs start only on SMs the GEMM leaves and
+        // claim whatever work is left -- so a collective that outlasts the
+        // GEMM widens onto its SMs, and one that finishes first leaves nothing
+        // for them but an immediate exit.
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
         const int comm_budget = part ? sm_split : p->comm_sms;
-        bool comm_launched = false;
-        auto go_gemm = [&] { return gemm_enqueue(gl, sg, ds.status, &gctas); };
+        cudaStream_t sc2 = ds.s_comm_b;
+        cudaEvent_t ev_c2 = ds.ev[6];
+        CopyGroup grp;
+        int cctas2 = 0;
+        bool comm_launched = false, rest_launched = false;
+        if (part && (e = cudaStreamWaitEvent(sc2, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        // Each completion event is recorded right after its own launch, before
+        // anything else is submitted.
+        auto go_gemm = [&] {
+            int r = gemm_enqueue(gl, sg, ds.status, &gctas);
+            if (r == C3_OK && (e = cudaEventRecord(ev_g, sg)) != cudaSuccess) r = set_cuda_error(e, "event record");
+            return r;
+        };
         auto go_comm = [&] {
-            int r = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas);
+            int r = launch_coll(ds, t, engine, p->sm_kernel, p->coll_l2, p->ce_variant, comm_budget, part, sc, &cctas,
+                                part ? ds.sm_count : 0, &grp);
             comm_launched = (r == C3_OK);
+            if (r == C3_OK && (e = cudaEventRecord(ev_c, sc)) != cudaSuccess) r = set_cuda_error(e, "event record");
+            return r;
+        };
+        auto go_rest = [&] {
+            if (!part) return (int)C3_OK;
+            int r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sc2,
+                                     &cctas2);
+            rest_launched = (r == C3_OK);
+            if (r == C3_OK && (e = cudaEventRecord(ev_c2, sc2)) != cudaSuccess) r = set_cuda_error(e, "event record");
             return r;
         };
         // A failure after the collective went out still orders the caller's
         // stream after it, so that the caller may reuse its buffers once its
-        // own stream has drained.
+        // own stream has drained; a split group missing its second part has
+        // its work counter cleared behind the first.
         auto fail = [&](int code) {
-            if (comm_launched && cudaEventRecord(ev_c, sc) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c, 0);
+            if (comm_launched) {
+                if (part && !rest_launched) abandon_group(grp, sc);
+                if (cudaEventRecord(ev_c, sc) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c, 0);
+            }
+            if (rest_launched && cudaEventRecord(ev_c2, sc2) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c2, 0);
             return code;
         };
         if (priority || reclaim) {
-            if ((rc = go_comm())) return rc;
+            if ((rc = go_comm())) return fail(rc);
             if ((rc = go_gemm())) return fail(rc);
         } else {
             if ((rc = go_gemm())) return rc;
-            if ((rc = go_comm())) return rc;
+            if ((rc = go_comm())) return fail(rc);
         }
-        if ((e = cudaEventRecord(ev_g, sg)) != cudaSuccess) return fail(set_cuda_error(e, "event record"));
-        if ((e = cudaEventRecord(ev_c, sc)) != cudaSuccess) return set_cuda_error(e, "event record");
+        if ((rc = go_rest())) return fail(rc);
         if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
+        if (part && (e = cudaStreamWaitEvent(s0, ev_c2, 0)) != cudaSuccess) return set_cuda_error(e, "join");
+        split_rest = part;
+        cctas += cctas2;
     }
     if ((e = cudaEventRecord(ev_end, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     if ((rc = wait_event(ev_end, 120.0))) return rc;
     out->t_gemm_ev = elapsed_s(ev0, ev_g);
     out->t_comm_ev = elapsed_s(ev0, ev_c);
+    if (split_rest) {
+        const double t2 = elapsed_s(ev0, ds.ev[6]);
+        if (t2 > out->t_comm_ev) out->t_comm_ev = t2;
+    }
     // From the start event to the later of the two completion events, each
     // recorded right after its kernel(s), as the isolated phases are timed;
     // the join that orders the caller's stream after both is not part of it.

@@ -61,55 +61,89 @@ __device__ __forceinline__ void st_vec_stream(uint8_t* p, uint4 v, uint64_t pol)
                  : "memory");
 }
 
-// Work unit of the vec kernel: a "round" of kVecThreads * kVecUnroll vectors
-// (64 KiB) inside one segment.  Rounds are dealt to CTAs grid-stride.
+// The last CTA of a launch group to finish puts the group's work counter back
+// to zero, so the slot is clean for its next user.
+__device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
+    __threadfence();
+    if (atomicAdd(&work[1], 1u) == (unsigned)total_ctas - 1u) {
+        atomicExch(&work[0], 0u);
+        atomicExch(&work[1], 0u);
+    }
+}
+
+// Work unit of the vec kernel: 64 KiB (4096 16-byte vectors) of one segment,
+// claimed by one warp from the group's counter (work[0]), so a CTA that shares
+// its SM with a GEMM CTA, or starts late because its SM was busy, simply moves
+// fewer units.  Lane 0 claims the warp's next unit while the current one is
+// copied and broadcasts it by shuffle; the kernel uses no shared memory, so it
+// still fits beside a GEMM CTA.  Within a unit every lane issues kVecUnroll
+// loads (each 512 contiguous bytes across the warp) before its stores.  A CTA
+// none of whose warps found work leaves at once and records no residency.
+constexpr uint64_t kVecUnit = 4096;  // vectors per unit (64 KiB)
+
 template <bool kStream>
 __global__ void __launch_bounds__(kVecThreads, 2)
-    copy_vec_kernel(SegTable t, DevStatus* st) {
-    if (threadIdx.x == 0) stamp_begin(st, false);
+    copy_vec_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas) {
+    const unsigned long long t_enter = globaltimer();
+    const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
-    constexpr uint64_t kRound = (uint64_t)kVecThreads * kVecUnroll;
-    const uint64_t rounds_per_seg = (vecs_per_seg + kRound - 1) / kRound;
-    const uint64_t total_rounds = rounds_per_seg * (uint64_t)t.nseg;
-    for (uint64_t r = blockIdx.x; r < total_rounds; r += gridDim.x) {
-        const uint64_t seg = r / rounds_per_seg;
-        const uint64_t v0 = (r - seg * rounds_per_seg) * kRound + threadIdx.x;
+    const uint64_t units_per_seg = (vecs_per_seg + kVecUnit - 1) / kVecUnit;
+    const uint64_t total_units = units_per_seg * (uint64_t)t.nseg;
+    unsigned c = 0;
+    if (lane == 0) c = atomicAdd(&work[0], 1u);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    const bool worked = c < total_units;
+    while (c < total_units) {
+        unsigned next = 0;
+        if (lane == 0) next = atomicAdd(&work[0], 1u);
+        const uint64_t seg = c / units_per_seg;
+        const uint64_t vbase = (c - seg * units_per_seg) * kVecUnit;
         const uint8_t* src = t.src[seg];
         uint8_t* dst = t.dst[seg];
-        uint4 v[kVecUnroll];
+#pragma unroll 1
+        for (uint64_t j = 0; j < kVecUnit; j += 32 * kVecUnroll) {
+            uint4 v[kVecUnroll];
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const uint64_t i = v0 + (uint64_t)u * kVecThreads;
-            if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
-        }
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const uint64_t i = vbase + j + (uint64_t)(u * 32 + lane);
+                if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
+            }
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const uint64_t i = v0 + (uint64_t)u * kVecThreads;
-            if (i < vecs_per_seg) {
-                if (kStream)
-                    st_vec_stream(dst + (i << 4), v[u], pol);
-                else
-                    st_vec(dst + (i << 4), v[u]);
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const uint64_t i = vbase + j + (uint64_t)(u * 32 + lane);
+                if (i < vecs_per_seg) {
+                    if (kStream)
+                        st_vec_stream(dst + (i << 4), v[u], pol);
+                    else
+                        st_vec(dst + (i << 4), v[u]);
+                }
             }
         }
+        c = __shfl_sync(0xffffffffu, next, 0);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) stamp_end(st, false);
+    // a hardware barrier reduction: did any warp of this CTA move a unit?
+    const int cta_worked = __syncthreads_or(worked ? 1 : 0);
+    if (threadIdx.x == 0) {
+        if (cta_worked) stamp_window(st, false, (unsigned)cta_base + blockIdx.x, t_enter, globaltimer());
+        group_done(work, total_ctas);
+    }
 }
 
 // bulk kernel: chunk c of the collective is segment c / chunks_per_seg at
 // byte offset (c % chunks_per_seg) * kBulkChunk (the last chunk of a segment
-// may be shorter; every size is a multiple of 16 bytes).
+// may be shorter; every size is a multiple of 16 bytes).  One thread claims
+// chunks from the group's counter as it issues their loads, remembers which
+// chunk each ring buffer holds, and stores them in the order loaded.
 template <bool kStream>
-__global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, DevStatus* st) {
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    copy_bulk_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kBulkBufs];
     __shared__ int abort_flag;
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
 
     if (threadIdx.x == 0) {
-        stamp_begin(st, false);
         abort_flag = 0;
         for (int b = 0; b < kBulkBufs; ++b) mbar_init(smem_addr(&full_bar[b]), 1);
         fence_barrier_init();
@@ -119,9 +153,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
         const uint64_t pol = kStream ? policy_evict_first() : 0;
         const uint64_t chunks_per_seg = (t.seg_bytes + kBulkChunk - 1) / kBulkChunk;
         const uint64_t total = chunks_per_seg * (uint64_t)t.nseg;
-        const uint64_t n_my = (blockIdx.x < total) ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-        auto chunk_of = [&](uint64_t i, const uint8_t*& src, uint8_t*& dst, uint32_t& bytes) {
-            const uint64_t c = blockIdx.x + i * gridDim.x;
+        const unsigned rec = (unsigned)cta_base + blockIdx.x;
+        uint32_t held[kBulkBufs];   // chunk id in each ring buffer
+        uint32_t issued = 0;        // loads issued (buffer issued % kBulkBufs next)
+        bool exhausted = false;
+        auto chunk_of = [&](uint32_t c, const uint8_t*& src, uint8_t*& dst, uint32_t& bytes) {
             const uint64_t seg = c / chunks_per_seg;
             const uint64_t off = (c - seg * chunks_per_seg) * kBulkChunk;
             const uint64_t left = t.seg_bytes - off;
@@ -129,57 +165,68 @@ __global__ void __launch_bounds__(kBulkThreads, 1) copy_bulk_kernel(SegTable t, 
             src = t.src[seg] + off;
             dst = t.dst[seg] + off;
         };
-        auto issue_load = [&](uint64_t i) {
+        // Claims the next chunk and issues its load into buffer issued % kBulkBufs.
+        auto try_issue = [&]() {
+            if (exhausted) return;
+            const uint32_t c = atomicAdd(&work[0], 1u);
+            if (c >= total) {
+                exhausted = true;
+                return;
+            }
+            if (issued == 0) stamp_begin(st, false, rec);
             const uint8_t* src;
             uint8_t* dst;
             uint32_t bytes;
-            chunk_of(i, src, dst, bytes);
-            const int b = (int)(i % kBulkBufs);
+            chunk_of(c, src, dst, bytes);
+            const int b = (int)(issued % kBulkBufs);
+            held[b] = c;
             const uint32_t bar = smem_addr(&full_bar[b]);
             mbar_arrive_expect_tx(bar, bytes);
             if (kStream)
                 bulk_load_hint(base + (uint32_t)b * kBulkChunk, src, bytes, bar, pol);
             else
                 bulk_load(base + (uint32_t)b * kBulkChunk, src, bytes, bar);
+            ++issued;
         };
-        const uint64_t pro = n_my < (uint64_t)kBulkBufs ? n_my : (uint64_t)kBulkBufs;
-        for (uint64_t i = 0; i < pro; ++i) issue_load(i);
-        uint64_t issued = pro;  // loads issued so far (chunks 0 .. issued-1)
-        uint64_t i = 0;
-        for (; i < n_my; ++i) {
-            const int b = (int)(i % kBulkBufs);
-            if (!mbar_wait(smem_addr(&full_bar[b]), (uint32_t)((i / kBulkBufs) & 1), &abort_flag)) {
+        for (int b = 0; b < kBulkBufs && !exhausted; ++b) try_issue();
+        uint32_t done = 0;  // chunks stored (in load order)
+        bool ok = true;
+        for (; done < issued; ++done) {
+            const int b = (int)(done % kBulkBufs);
+            if (!mbar_wait(smem_addr(&full_bar[b]), (done / kBulkBufs) & 1u, &abort_flag)) {
                 report_error(st, -4, kSiteBulkLoad);
+                ok = false;
                 break;
             }
             const uint8_t* src;
             uint8_t* dst;
             uint32_t bytes;
-            chunk_of(i, src, dst, bytes);
+            chunk_of(held[b], src, dst, bytes);
             if (kStream)
                 bulk_store_hint(dst, base + (uint32_t)b * kBulkChunk, bytes, pol);
             else
                 bulk_store(dst, base + (uint32_t)b * kBulkChunk, bytes);
             bulk_commit();
-            // Refill the buffer of chunk i-1 once its store has read it.
-            if (i >= 1 && i - 1 + kBulkBufs < n_my) {
+            // Refill the buffer of chunk done-1 (the one the next load goes to)
+            // once its store has read it.
+            if (done >= 1 && !exhausted) {
                 bulk_wait_read<1>();
-                issue_load(i - 1 + kBulkBufs);
-                ++issued;
+                try_issue();
             }
         }
-        if (i < n_my) {
+        if (!ok) {
             // Gave up: let every load still in flight land before the CTA's
             // shared memory is released.
-            for (uint64_t j = i; j < issued; ++j) {
+            for (uint32_t j = done; j < issued; ++j) {
                 const int b = (int)(j % kBulkBufs);
                 volatile int dummy = 0;
-                if (!mbar_wait(smem_addr(&full_bar[b]), (uint32_t)((j / kBulkBufs) & 1), &dummy))
+                if (!mbar_wait(smem_addr(&full_bar[b]), (j / kBulkBufs) & 1u, &dummy))
                     report_error(st, -4, kSiteBulkDrain);
             }
         }
         bulk_wait_all();
-        stamp_end(st, false);
+        if (issued > 0) stamp_end(st, false, rec);
+        group_done(work, total_ctas);
     }
     __syncthreads();
 }
@@ -248,22 +295,42 @@ int copy_init_device(int max_reserve) {
     return 0;
 }
 
-int copy_sm_launch(const SegTable& t, int ctas, int flavour, int smem_reserve, int l2_stream, cudaStream_t s,
-                   DevStatus* st, int* ctas_out) {
+CopyGroup copy_group(DeviceState& ds, int total_ctas) {
+    CopyGroup g;
+    g.work = ds.status->coll_sched[ds.next_coll_sched++ % kSchedSlots];
+    g.total_ctas = total_ctas;
+    return g;
+}
+
+static uint64_t copy_units(const SegTable& t, uint64_t unit_bytes) {
+    return (t.seg_bytes + unit_bytes - 1) / unit_bytes * (uint64_t)t.nseg;
+}
+
+bool copy_units_fit(const SegTable& t) {
+    // 32 KiB chunks are the smaller unit; keep the count (plus one overshooting
+    // claim per CTA) well inside 32 bits
+    return copy_units(t, kBulkChunk) < (1ull << 31);
+}
+
+int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
+    if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas)
+        return set_error(-1, "copy launch group does not cover this launch");
+    if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 32 KiB chunks");
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
-    if (ctas < 1) ctas = 1;
+    if (ctas < 1) return set_error(-1, "copy launch needs at least one CTA");
     if (flavour == kSmkBulk) {
         if (l2_stream)
-            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st);
+            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas);
         else
-            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st);
+            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas);
     } else {
         if (l2_stream)
-            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas);
         else
-            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st);
+            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "copy kernel launch");

@@ -111,6 +111,13 @@ def test_injected_failure_inside_a_concurrent_run(mode, site, priority):
     out.zero_()
     r = c3.c3_run(p, mode, split, 0)
     assert r["status"] == 0 and gemm_ok() and coll_ok()
+    # every collective work counter is clean: a run whose second launch part
+    # never went out had its counter cleared, so the slots (64, round robin)
+    # serve later launches correctly
+    for i in range(70):
+        out.zero_()
+        c3.c3_allgather(ds, out, sb, 8, engine=c3.C3_ENGINE_SM, sm_budget=1 + i % 5)
+        assert coll_ok(), i
 
 
 def test_injected_device_init_failure_and_reinit():

@@ -101,8 +101,9 @@ def test_partitioned_runs_on_disjoint_sms(c3, setup, split):
     t = c3.c3_run(setup.p, 1, split, 0)
     # no SM ever held a GEMM CTA and a collective CTA at the same time
     assert t["smid_overlap"] == 0, t
-    assert t["comm_sms"] <= split
     assert t["gemm_ctas"] <= info["sm_count"] - split
+    # one launch group of SM-count CTAs: split now, the rest on SMs the GEMM leaves
+    assert t["comm_ctas"] == info["sm_count"]
     setup.verify()
 
 
@@ -110,10 +111,56 @@ def test_partitioned_runs_on_disjoint_sms(c3, setup, split):
 def test_reclaim_never_shares_an_sm_at_once(c3, setup, split):
     # the GEMM may reuse the collective's SMs after it leaves, never during
     setup.poison()
+    info = c3.c3_get_device_info()
     t = c3.c3_run(setup.p, 4, split, 0)
     assert t["smid_overlap"] == 0, t
-    assert t["comm_sms"] <= split
+    assert t["comm_ctas"] == info["sm_count"]
     setup.verify()
+
+
+@pytest.mark.parametrize("mode,prio", [(1, 0), (1, 1), (4, 0)])
+@pytest.mark.parametrize("flavour", [0, 1])   # auto (bulk when exclusive), vec with a reservation
+def test_partitioned_collective_widens_onto_the_sms_the_gemm_leaves(c3, mode, prio, flavour):
+    """A one-tile GEMM beside a 256 MiB all-gather partitioned onto 8 SMs: the
+    GEMM leaves ~140 SMs idle, so the collective's second launch part takes
+    them and claims most of the work; the output stays bit-exact and no SM
+    ever holds both kernels at once."""
+    info = c3.c3_get_device_info()
+    M, N, K = 128, 128, 64
+    A = I.bf16_uniform(21, (M, K))
+    B = I.bf16_uniform(22, (N, K))
+    C_ref, S_ref = oracle.gemm(A, B)
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    unit = 32 << 20
+    shards = [torch.randint(0, 256, (unit,), dtype=torch.uint8, device="cuda") for _ in range(8)]
+    out = torch.zeros(8 * unit, dtype=torch.uint8, device="cuda")
+    ref = torch.cat(shards)
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLGATHER, out, unit, 8, shards=shards, sm_kernel=flavour)
+    t = c3.c3_run(p, mode, 8, prio)
+    assert t["status"] == 0
+    assert torch.equal(out, ref)
+    assert (np.abs(dC.cpu().numpy().astype(np.float64) - C_ref) <= TOL * S_ref).all()
+    assert t["smid_overlap"] == 0, t
+    assert t["comm_ctas"] == info["sm_count"]
+    # 8 SMs alone would need ~3 ms for 512 MiB of traffic; the idle SMs join at once
+    assert t["comm_sms"] > 64, t
+
+
+def test_copy_work_counters_recycle_over_many_launches(c3):
+    """More collective launches than work-counter slots (64), with launch
+    groups of 1..7 CTAs: a counter left non-zero would make a later launch
+    skip work, so every output is compared with the expected bytes."""
+    unit = (1 << 20) + 48
+    shards = [torch.randint(0, 256, (unit,), dtype=torch.uint8, device="cuda") for _ in range(8)]
+    ref = torch.cat(shards)
+    out = torch.empty(8 * unit, dtype=torch.uint8, device="cuda")
+    for i in range(150):
+        out.fill_(0xA5)
+        c3.c3_allgather(shards, out, unit, 8, engine=c3.C3_ENGINE_SM, sm_budget=1 + i % 7)
+        assert torch.equal(out, ref), i
+    c3.c3_status_check()
 
 
 def test_scheduler_slots_recycle_over_many_launches(c3):
