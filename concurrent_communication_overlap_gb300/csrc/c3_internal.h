@@ -147,12 +147,16 @@ int gemm_init_device();  // function attributes; once per device
 
 // A group of SM copy launches sharing one work counter: `total_ctas` CTAs over
 // every launch of the group; each launch numbers its CTAs from `cta_base`.
+// The first part (CTAs 0 .. static_ctas-1, launched first) starts on fixed
+// work units; every later unit is claimed from the counter.
 struct CopyGroup {
     unsigned int* work = nullptr;  // DevStatus::coll_sched slot
     int total_ctas = 0;
+    int static_ctas = 0;
 };
-// Picks the next work-counter slot of the device (round robin).
-CopyGroup copy_group(DeviceState& ds, int total_ctas);
+// Picks the next work-counter slot of the device (round robin) for a group of
+// total_ctas CTAs whose first launch part has first_ctas CTAs.
+CopyGroup copy_group(DeviceState& ds, int total_ctas, int first_ctas);
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
                    int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out);
 // Largest number of work units (64 KiB rounds / 32 KiB chunks) a collective may

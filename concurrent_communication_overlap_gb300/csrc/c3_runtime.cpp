@@ -351,7 +351,7 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
         if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
         const int flavour = pick_flavour(t, sm_kernel, exclusive);
         const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-        CopyGroup g = copy_group(ds, total);
+        CopyGroup g = copy_group(ds, total, k);
         if (group) *group = g;
         int dummy = 0;
         return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, &dummy);
@@ -359,7 +359,7 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
     if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
     const int flavour = pick_flavour(t, sm_kernel, exclusive);
     const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-    CopyGroup g = copy_group(ds, total);
+    CopyGroup g = copy_group(ds, total, k);
     if (group) *group = g;
     return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, ctas);
 }

@@ -71,32 +71,40 @@ __device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
     }
 }
 
-// Work unit of the vec kernel: 64 KiB (4096 16-byte vectors) of one segment,
-// claimed by one warp from the group's counter (work[0]), so a CTA that shares
-// its SM with a GEMM CTA, or starts late because its SM was busy, simply moves
-// fewer units.  Lane 0 claims the warp's next unit while the current one is
-// copied and broadcasts it by shuffle; the kernel uses no shared memory, so it
-// still fits beside a GEMM CTA.  Within a unit every lane issues kVecUnroll
-// loads (each 512 contiguous bytes across the warp) before its stores.  A CTA
-// none of whose warps found work leaves at once and records no residency.
-constexpr uint64_t kVecUnit = 4096;  // vectors per unit (64 KiB)
+// Work unit of the vec kernel: 16 KiB (1024 16-byte vectors, four passes of
+// kVecUnroll vectors per lane) of one segment, moved by one warp.  Warp w of
+// the group's first launch part (w = CTA index in the group * 16 + warp) takes
+// unit w without asking; every other unit is claimed from the group's counter
+// (work[0]), numbered after those, so a warp that shares its SM with a GEMM
+// CTA, or a CTA that starts late because its SM was busy, simply moves fewer
+// units.  Lane 0 claims the warp's next unit while the current one is copied
+// and broadcasts it by shuffle.  Within a pass every lane issues kVecUnroll
+// loads (each 512 contiguous bytes across the warp) before its stores.  The
+// kernel uses no shared memory, so it still fits beside a GEMM CTA.  A CTA none
+// of whose warps found work leaves at once and records no residency.
+constexpr uint64_t kVecUnit = 1024;  // vectors per unit (16 KiB)
+constexpr int kVecWarps = kVecThreads / 32;
 
 template <bool kStream>
 __global__ void __launch_bounds__(kVecThreads, 2)
-    copy_vec_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas) {
+    copy_vec_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
+                    unsigned static_units) {
     const unsigned long long t_enter = globaltimer();
     const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
     const uint64_t units_per_seg = (vecs_per_seg + kVecUnit - 1) / kVecUnit;
     const uint64_t total_units = units_per_seg * (uint64_t)t.nseg;
-    unsigned c = 0;
-    if (lane == 0) c = atomicAdd(&work[0], 1u);
-    c = __shfl_sync(0xffffffffu, c, 0);
+    const unsigned gwarp = ((unsigned)cta_base + blockIdx.x) * kVecWarps + (threadIdx.x >> 5);
+    unsigned c = gwarp;
+    if (gwarp >= static_units) {
+        if (lane == 0) c = static_units + atomicAdd(&work[0], 1u);
+        c = __shfl_sync(0xffffffffu, c, 0);
+    }
     const bool worked = c < total_units;
     while (c < total_units) {
         unsigned next = 0;
-        if (lane == 0) next = atomicAdd(&work[0], 1u);
+        if (lane == 0) next = static_units + atomicAdd(&work[0], 1u);
         const uint64_t seg = c / units_per_seg;
         const uint64_t vbase = (c - seg * units_per_seg) * kVecUnit;
         const uint8_t* src = t.src[seg];
@@ -137,7 +145,8 @@ __global__ void __launch_bounds__(kVecThreads, 2)
 // chunk each ring buffer holds, and stores them in the order loaded.
 template <bool kStream>
 __global__ void __launch_bounds__(kBulkThreads, 1)
-    copy_bulk_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas) {
+    copy_bulk_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
+                     unsigned static_units) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kBulkBufs];
     __shared__ int abort_flag;
@@ -166,9 +175,15 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             dst = t.dst[seg] + off;
         };
         // Claims the next chunk and issues its load into buffer issued % kBulkBufs.
+        // A CTA of the group's first launch part takes chunks b * kBulkBufs ..
+        // b * kBulkBufs + kBulkBufs - 1 (b its index in the group) without
+        // asking; every other chunk comes from the counter, numbered after those.
+        const uint32_t first = ((unsigned)cta_base + blockIdx.x) * (uint32_t)kBulkBufs;
         auto try_issue = [&]() {
             if (exhausted) return;
-            const uint32_t c = atomicAdd(&work[0], 1u);
+            const uint32_t c = (first < static_units && issued < (uint32_t)kBulkBufs)
+                                   ? first + issued
+                                   : static_units + atomicAdd(&work[0], 1u);
             if (c >= total) {
                 exhausted = true;
                 return;
@@ -295,10 +310,11 @@ int copy_init_device(int max_reserve) {
     return 0;
 }
 
-CopyGroup copy_group(DeviceState& ds, int total_ctas) {
+CopyGroup copy_group(DeviceState& ds, int total_ctas, int first_ctas) {
     CopyGroup g;
     g.work = ds.status->coll_sched[ds.next_coll_sched++ % kSchedSlots];
     g.total_ctas = total_ctas;
+    g.static_ctas = first_ctas;
     return g;
 }
 
@@ -316,21 +332,25 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
                    int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
-    if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas)
+    if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas || g.static_ctas < 0 ||
+        g.static_ctas > g.total_ctas || (cta_base > 0 && cta_base < g.static_ctas))
         return set_error(-1, "copy launch group does not cover this launch");
     if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 32 KiB chunks");
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) return set_error(-1, "copy launch needs at least one CTA");
+    // the group's first part (its first g.static_ctas CTAs) starts on fixed units
     if (flavour == kSmkBulk) {
+        const unsigned su = (unsigned)g.static_ctas * (unsigned)kBulkBufs;
         if (l2_stream)
-            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas);
+            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
         else
-            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas);
+            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
     } else {
+        const unsigned su = (unsigned)g.static_ctas * (unsigned)kVecWarps;
         if (l2_stream)
-            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas);
+            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
         else
-            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas);
+            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "copy kernel launch");
