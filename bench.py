@@ -818,13 +818,15 @@ def main(argv=None):
     flush = torch.empty(2 * info["l2_bytes"] + (16 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     peaks = load_peaks()
-    # the settle period, from the GEMM's isolated time (after two untimed launches)
-    for _ in range(2):
-        c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
-    t_g0, _ = _event_time(torch, stream, lambda: c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream), 3, 0,
-                          lambda: c3.c3_l2_flush(flush, flush.numel(), stream))
-    settle_us = auto_settle_us(t_g0, args.settle_ms)
-    plateaus = {} if host_src else measure_plateaus(c3, torch, w, dev, stream, flush)
+    settle_us, plateaus = 0, {}
+    if not args.profile_range:
+        # the settle period, from the GEMM's isolated time (after two untimed launches)
+        for _ in range(2):
+            c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream)
+        t_g0, _ = _event_time(torch, stream, lambda: c3.c3_gemm(dA, dB, dC, w.M, w.N, w.K, 0, stream), 3, 0,
+                              lambda: c3.c3_l2_flush(flush, flush.numel(), stream))
+        settle_us = auto_settle_us(t_g0, args.settle_ms)
+        plateaus = {} if host_src else measure_plateaus(c3, torch, w, dev, stream, flush)
     prob = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
                       send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
                       ce_variant=ce_variant_arg(args, c3), settle_us=settle_us,

@@ -357,40 +357,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t wstg =
                     stg + (uint32_t)q * (Cfg::kOwnStaging ? 8192u : (uint32_t)Cfg::kRingBlocksPerWarp * 4096u);
                 int issued = 0;
-#pragma unroll 1
-                for (int sub = 0; sub < MSUB; ++sub) {
+                // The 32 x 32 pieces j = 0 .. MSUB * BN/32 - 1 (sub-tile j / (BN/32),
+                // column block j % (BN/32)) are read out of TMEM one ahead of the one
+                // being staged: the load of piece j+1 is in flight while piece j goes
+                // to shared memory, and the accumulator set is released as soon as its
+                // last piece has landed in registers.
+                constexpr int kPieces = MSUB * (BN / 32);
+                const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * Cfg::kAccCols);
+                auto piece_taddr = [&](int j) {
+                    return tq + (uint32_t)((j / (BN / 32)) * BN + (j % (BN / 32)) * 32);
+                };
+                auto release_if_last = [&](int j_landed) {
+                    if (j_landed == kPieces - 1) {
+                        // the accumulator set has been read out: the MMA may reuse it
+                        tc_fence_before();
+                        mbar_arrive(bar(BAR_TEMPTY + buf));
+                    }
+                };
+                auto stage_piece = [&](const uint32_t (&r)[32], int j) {
+                    const int sub = j / (BN / 32), c = j % (BN / 32);
                     const int row0 = mb * kRowsCta + sub * kBM + q * 32;
-                    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                           (uint32_t)(buf * Cfg::kAccCols + sub * BN);
-#pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(taddr + (uint32_t)(c * 32), r);
-                        tmem_ld_wait();
-                        if (sub == MSUB - 1 && c == BN / 32 - 1) {
-                            // the accumulator set has been read out: the MMA may reuse it
-                            tc_fence_before();
-                            mbar_arrive(bar(BAR_TEMPTY + buf));
-                        }
-                        const int col0 = nb * BN + c * 32;
-                        if (row0 >= M || col0 >= N) continue;  // wholly outside C (uniform per warp)
-                        const uint32_t blk = wstg + (uint32_t)(Cfg::kOwnStaging ? (issued & 1) : issued) * 4096u;
-                        if (Cfg::kOwnStaging && issued >= 2) {
-                            if (lane == 0) bulk_wait_read<1>();
-                            __syncwarp();
-                        }
-                        const uint32_t rowp = blk + (uint32_t)lane * 128u;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_shared_v4(rowp + ((uint32_t)(j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1],
-                                         r[4 * j + 2], r[4 * j + 3]);
-                        fence_proxy_async_smem();
+                    const int col0 = nb * BN + c * 32;
+                    if (row0 >= M || col0 >= N) return;  // wholly outside C (uniform per warp)
+                    const uint32_t blk = wstg + (uint32_t)(Cfg::kOwnStaging ? (issued & 1) : issued) * 4096u;
+                    if (Cfg::kOwnStaging && issued >= 2) {
+                        if (lane == 0) bulk_wait_read<1>();
                         __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmC, blk, col0, row0);  // clipped to M x N by the tensor map
-                            bulk_commit();
-                        }
-                        ++issued;
+                    }
+                    const uint32_t rowp = blk + (uint32_t)lane * 128u;
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        st_shared_v4(rowp + ((uint32_t)(jj ^ (lane & 7)) << 4), r[4 * jj], r[4 * jj + 1],
+                                     r[4 * jj + 2], r[4 * jj + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, blk, col0, row0);  // clipped to M x N by the tensor map
+                        bulk_commit();
+                    }
+                    ++issued;
+                };
+                uint32_t ra[32], rb[32];
+                tmem_ld32(piece_taddr(0), ra);
+                tmem_ld_wait();
+                release_if_last(0);
+#pragma unroll 1
+                for (int j = 0; j < kPieces; j += 2) {
+                    // ra holds piece j; rb receives piece j+1 meanwhile
+                    if (j + 1 < kPieces) tmem_ld32(piece_taddr(j + 1), rb);
+                    stage_piece(ra, j);
+                    if (j + 1 >= kPieces) break;
+                    tmem_ld_wait();
+                    release_if_last(j + 1);
+                    if (j + 2 < kPieces) tmem_ld32(piece_taddr(j + 2), ra);
+                    stage_piece(rb, j + 1);
+                    if (j + 2 < kPieces) {
+                        tmem_ld_wait();
+                        release_if_last(j + 2);
                     }
                 }
                 if (lane == 0) bulk_wait_read<0>();  // staging free for the next tile
