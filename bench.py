@@ -899,6 +899,7 @@ def main(argv=None):
         return c_ok, g_ok
 
     coll_ok, gemm_ok = outputs_ok()
+    spread_ctas = gemm_cta_spread(c3, prob)
     per_mode_ok = {}
     for name, mode, split, prio in modes:
         out.fill_(0xA5)
@@ -1039,6 +1040,7 @@ def main(argv=None):
                                     for k, v in per_mode_ok.items()},
                        "gemm_rows": [int(r) for r in rows]},
         "modes": stats,
+        "gemm_cta_spread": spread_ctas,
         "device": {"name": torch.cuda.get_device_name(dev), **info},
     }
     detail["clocks"] = clk.summary()
@@ -1158,6 +1160,25 @@ def _event_time(torch, stream, fn, reps, warm, flush=None):
         e1.synchronize()
         ts.append(e0.elapsed_time(e1) * 1e-3)
     return statistics.fmean(ts), ts
+
+
+def gemm_cta_spread(c3, prob, runs=5):
+    """How evenly the GEMM's CTAs finish when it runs alone: a serial-mode run
+    (the GEMM first, nothing beside it), then the per-CTA %globaltimer windows
+    of its CTAs.  Per run: the spread of CTA end times (median to last), the
+    last CTA's end, and the mean CTA duration; medians over `runs` runs."""
+    rows = []
+    for _ in range(runs):
+        c3.c3_run(prob, c3.C3_MODE_SERIAL_SM, 0, 0)
+        w = c3.c3_cta_windows(0)
+        if not w:
+            return None
+        ends = sorted(t1 for _, _, _, t1 in w)
+        rows.append({"ctas": len(w), "end_min_us": 1e6 * ends[0], "end_median_us": 1e6 * statistics.median(ends),
+                     "end_max_us": 1e6 * ends[-1],
+                     "tail_us": 1e6 * (ends[-1] - statistics.median(ends)),
+                     "distinct_sms": len({sm for _, sm, _, _ in w})})
+    return {k: statistics.median(r[k] for r in rows) for k in rows[0]}
 
 
 def measure_plateaus(c3, torch, w, dev, stream, flush):

@@ -68,6 +68,10 @@ class C3Timing(ctypes.Structure):
         return d
 
 
+class C3CtaWindow(ctypes.Structure):
+    _fields_ = [("cta", _int), ("smid", _int), ("t_start", ctypes.c_double), ("t_end", ctypes.c_double)]
+
+
 C3_RP_MAX = 16
 
 
@@ -108,6 +112,7 @@ def _load():
                           ctypes.c_double, ctypes.c_double, ctypes.POINTER(_int), ctypes.POINTER(ctypes.c_double),
                           ctypes.POINTER(ctypes.c_double)],
         "c3_gemm_plan": [_i64, _i64, _i64, _int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)],
+        "c3_cta_windows": [_int, ctypes.POINTER(C3CtaWindow), _int, ctypes.POINTER(_int)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -124,7 +129,7 @@ _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_allreduce", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
             "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_inject_fault", "c3_sp_predict",
-            "c3_rp_predict")
+            "c3_rp_predict", "c3_cta_windows")
 
 
 def lib():
@@ -213,6 +218,14 @@ def c3_gemm_plan(M, N, K, sm_budget=0):
     _check(_lib.c3_gemm_plan(int(M), int(N), int(K), int(sm_budget), ctypes.byref(bn), ctypes.byref(ms),
                              ctypes.byref(ctas)), "c3_gemm_plan")
     return bn.value, ms.value, ctas.value
+
+
+def c3_cta_windows(kernel):
+    """[(cta, smid, t_start_s, t_end_s)] of the last run's GEMM (0) or SM collective (1) CTAs."""
+    arr = (C3CtaWindow * 256)()
+    n = _int()
+    _check(_lib.c3_cta_windows(int(kernel), arr, 256, ctypes.byref(n)), "c3_cta_windows")
+    return [(arr[i].cta, arr[i].smid, arr[i].t_start, arr[i].t_end) for i in range(n.value)]
 
 
 def c3_selftest_wait(limit_ns, arrive, stream=None):

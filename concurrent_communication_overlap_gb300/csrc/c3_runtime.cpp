@@ -809,6 +809,34 @@ int c3_alltoall(const void* in, void* out, size_t block_bytes, int nranks, int e
     return launch_coll(*ds, t, engine, C3_SMK_AUTO, 0, kCeGraph, sm_budget, false, static_cast<cudaStream_t>(s), nullptr);
 }
 
+int c3_cta_windows(int kernel, c3_cta_window* out, int max, int* n) {
+    if (kernel != 0 && kernel != 1) return set_error(C3_EINVAL, "kernel must be 0 (GEMM) or 1 (SM collective)");
+    if (!out || !n || max < 0) return set_error(C3_EINVAL, "out, n and max >= 0 are required");
+    *n = 0;
+    DeviceState* ds = device_state();
+    if (!ds) return C3_ECUDA;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return set_cuda_error(e, "device synchronize");
+    static DevStatus h;  // 12+ KiB: not on the stack
+    e = cudaMemcpy(&h, ds->status, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_cuda_error(e, "reading the status block");
+    const CtaRec* recs = kernel == 0 ? h.gemm_rec : h.comm_rec;
+    unsigned long long t0 = ~0ull;
+    for (int i = 0; i < kCtaRecs; ++i)
+        if (recs[i].used && recs[i].t0 < t0) t0 = recs[i].t0;
+    int k = 0;
+    for (int i = 0; i < kCtaRecs && k < max; ++i) {
+        if (!recs[i].used) continue;
+        out[k].cta = i;
+        out[k].smid = (int)recs[i].smid;
+        out[k].t_start = (double)(recs[i].t0 - t0) * 1e-9;
+        out[k].t_end = (double)(recs[i].t1 - t0) * 1e-9;
+        ++k;
+    }
+    *n = k;
+    return C3_OK;
+}
+
 int c3_inject_fault(int site) {
     if (site < C3_FAULT_NONE || site > C3_FAULT_DEVICE_INIT) return set_error(C3_EINVAL, "unknown fault site");
     g_fault.store(site);

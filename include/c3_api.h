@@ -470,6 +470,29 @@ int c3_rp_predict(const c3_rp_table *t, double gemm_flops, double gemm_bytes, do
                   double peak_flops, double peak_bytes_per_s, int *best_sms, double *t_pred_best,
                   double *t_pred_each);
 
+/*
+ * Per-CTA windows of the last run (diagnostics; the pages have no
+ * counterpart).  Every CTA of the GEMM kernel and of the SM collective
+ * records the SM it ran on and its %globaltimer start and end in the
+ * library's status block; c3_run (and the concurrent phase ending each
+ * c3_time repetition) clears the block first, so after a c3_run these are
+ * that run's kernels.  A c3_run in a serial mode gives the GEMM's CTAs timed
+ * alone.  Collective CTAs that found no work left record nothing.
+ *   kernel  0: the GEMM's CTAs; 1: the SM collective's CTAs
+ *   out     host array of `max` entries, filled in CTA order (the first 256
+ *           CTAs of a launch are recorded); times in seconds from the
+ *           earliest start among the recorded CTAs of that kernel
+ *   *n      receives the number of entries written
+ * Synchronises the device.  C3_EINVAL on a bad kernel index or NULL output.
+ */
+typedef struct {
+    int cta;          /* CTA index within its launch group */
+    int smid;         /* %smid of the SM it ran on */
+    double t_start;   /* seconds from the kernel's first recorded CTA start */
+    double t_end;
+} c3_cta_window;
+int c3_cta_windows(int kernel, c3_cta_window *out, int max, int *n);
+
 /* The L2 flush used between timed phases: writes `bytes` of zeros over `buf`
  * (device), then reads back its first half, so that L2 ends up holding clean
  * lines (a write-only flush would leave L2 full of dirty lines whose

@@ -115,6 +115,11 @@ def test_argument_errors_before_any_cuda_call(c3):
     assert c3.lib().c3_inject_fault(-1) == c3.C3_EINVAL
     assert c3.lib().c3_inject_fault(c3.C3_FAULT_GEMM_LAUNCH) == c3.C3_OK
     assert c3.lib().c3_inject_fault(c3.C3_FAULT_NONE) == c3.C3_OK   # disarmed again
+    n = ctypes.c_int()
+    arr = (c3.C3CtaWindow * 4)()
+    assert c3.lib().c3_cta_windows(2, arr, 4, ctypes.byref(n)) == c3.C3_EINVAL
+    assert c3.lib().c3_cta_windows(0, None, 4, ctypes.byref(n)) == c3.C3_EINVAL
+    assert c3.lib().c3_cta_windows(0, arr, -1, ctypes.byref(n)) == c3.C3_EINVAL
 
 
 def test_run_and_time_reject_bad_records(c3):

@@ -235,3 +235,19 @@ def test_timer_bounds_and_settle_follow_their_definitions(c3, setup, plateau_sca
     # no peaks, no plateau: both axes unknown
     r = c3.c3_time(setup.p, 1, 0, 0, warmup=0, reps=1)[0]
     assert r["gemm_bound"] == c3.C3_BOUND_UNKNOWN and r["coll_bound"] == c3.C3_BOUND_UNKNOWN
+
+
+def test_cta_windows_describe_the_last_run(c3, setup):
+    """After a serial run, the GEMM's per-CTA windows: one per launched CTA,
+    each on its own SM, ordered start <= end, starting from zero; the
+    collective's windows belong to CTAs that moved data."""
+    t = c3.c3_run(setup.p, 0, 0, 0)
+    g = c3.c3_cta_windows(0)
+    assert len(g) == t["gemm_ctas"]
+    assert len({sm for _, sm, _, _ in g}) == len(g)
+    assert min(t0 for _, _, t0, _ in g) == 0.0
+    assert all(0.0 <= t0 <= t1 for _, _, t0, t1 in g)
+    assert max(t1 for _, _, _, t1 in g) <= t["t_gemm_ev"]
+    cw = c3.c3_cta_windows(1)
+    assert 1 <= len(cw) <= t["comm_ctas"]
+    assert all(t0 <= t1 for _, _, t0, t1 in cw)
