@@ -54,3 +54,42 @@ def test_rp_rejects_bad_tables(c3):
         c3.c3_rp_predict([(8, 0.0, 1.0, 1.0)], 1e12, 1e9, 1e8, 1e15, 1e12)
     with pytest.raises(c3.C3Error):
         c3.c3_rp_predict([(8, 1.0, 1.0, 1.0)], 1e12, 0.0, 1e8, 1e15, 1e12)
+
+
+def _record():
+    """The GB300 validation record committed with the profiles: slowdown table,
+    peaks and, per scenario, the measured T_conc of each split and the split
+    the heuristic predicted."""
+    import json
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles", "heuristics_rp.md")
+    text = open(path).read()
+    return json.loads(re.search(r"```json\n(.*?)\n```", text, re.S).group(1))
+
+
+def test_recorded_predictions_are_reproduced_from_the_committed_table(c3):
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from concurrent_communication_overlap_gb300 import inputs as I
+    rec = _record()
+    table = [(e["sms"], e["gemm_compute"], e["gemm_memory"], e["coll"]) for e in rec["table"]]
+    pf, pb = rec["peaks"]["bf16_tflops"] * 1e12, rec["peaks"]["hbm_gbs"] * 1e9
+    assert len(rec["rows"]) == rec["scenarios"] == 29
+    hits = 0
+    for row in rec["rows"]:
+        w = bench.find_workload(I, row["scenario"])
+        best_pred, _, _ = c3.c3_rp_predict(table, w.gemm_flops, w.gemm_bytes, w.coll_bytes, pf, pb)
+        assert best_pred == row["predicted_sms"], row["scenario"]
+        # recount the verdict from the measured times: the swept best, the loss, the 1.5% rule
+        t = {int(k): v for k, v in row["t_conc_us"].items()}
+        best = min(t, key=t.get)
+        assert best == row["best_sms"], row["scenario"]
+        loss = t[best_pred] / t[best] - 1.0
+        assert loss == pytest.approx(row["loss_pct"] / 100.0, abs=1e-4)
+        hit = best_pred == best or loss <= 0.015
+        assert hit == row["hit"], row["scenario"]
+        hits += hit
+    assert hits == rec["hits"] == 24   # the pages' own bar: 24 of 30 (Section V-C)
