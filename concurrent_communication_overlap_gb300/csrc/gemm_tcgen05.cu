@@ -527,7 +527,8 @@ struct TileCfg {
     int bn, msub, stages, acc_bufs, smem;
 };
 #define C3_CFG(BN_, MS_) {BN_, MS_, GemmCfg<BN_, MS_>::kStages, GemmCfg<BN_, MS_>::kAccBufs, GemmCfg<BN_, MS_>::kSmem}
-static const TileCfg kCfgs[] = {C3_CFG(256, 1), C3_CFG(128, 1), C3_CFG(256, 2), C3_CFG(192, 2), C3_CFG(128, 2)};
+static const TileCfg kCfgs[] = {C3_CFG(256, 1), C3_CFG(128, 1), C3_CFG(256, 2), C3_CFG(224, 2), C3_CFG(192, 2),
+                                C3_CFG(128, 2)};
 #undef C3_CFG
 constexpr int kNumCfgs = sizeof(kCfgs) / sizeof(kCfgs[0]);
 
@@ -547,6 +548,7 @@ int gemm_init_device() {
     cudaError_t e = set_attr<256, 1>();
     if (e == cudaSuccess) e = set_attr<128, 1>();
     if (e == cudaSuccess) e = set_attr<256, 2>();
+    if (e == cudaSuccess) e = set_attr<224, 2>();
     if (e == cudaSuccess) e = set_attr<192, 2>();
     if (e == cudaSuccess) e = set_attr<128, 2>();
     if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(gemm)");
@@ -594,6 +596,7 @@ static int launch_cfg(int ci, int grid, const CUtensorMap& ma, const CUtensorMap
     if (c.bn == 256 && c.msub == 1) C3_LAUNCH(256, 1);
     else if (c.bn == 128 && c.msub == 1) C3_LAUNCH(128, 1);
     else if (c.bn == 256 && c.msub == 2) C3_LAUNCH(256, 2);
+    else if (c.bn == 224 && c.msub == 2) C3_LAUNCH(224, 2);
     else if (c.bn == 192 && c.msub == 2) C3_LAUNCH(192, 2);
     else C3_LAUNCH(128, 2);
 #undef C3_LAUNCH

@@ -62,6 +62,8 @@ def assert_gemm_close(C_gpu, C_ref, S_ref):
     (400, 700, 520, 2, (256, 2)),      # two 128-row sub-tiles per CTA, one accumulator set
     (400, 1100, 200, 2, (128, 2)),     # two sub-tiles, two accumulator sets
     (400, 1100, 520, 4, (192, 2)),     # the memory-bound workload's configuration
+    (300, 1000, 520, 5, (224, 2)),     # the configuration the memory-bound GEMM takes on 128-144 SMs
+    (256, 1792, 1032, 8, (224, 2)),
     # degenerate shapes: boxes far larger than the tensor on one or both sides
     (1, 1, 8, 0, None),                # a single output (scalar store path)
     (1, 4096, 64, 0, None),            # one row of C, TMA-stored
