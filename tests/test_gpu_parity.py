@@ -62,7 +62,7 @@ def assert_gemm_close(C_gpu, C_ref, S_ref):
     (400, 700, 520, 2, (256, 2)),      # two 128-row sub-tiles per CTA, one accumulator set
     (400, 1100, 200, 2, (128, 2)),     # two sub-tiles, two accumulator sets
     (400, 1100, 520, 4, (192, 2)),     # the memory-bound workload's configuration
-    (300, 1000, 520, 5, (224, 2)),     # the configuration the memory-bound GEMM takes on 128-144 SMs
+    (256, 1000, 520, 5, (224, 2)),     # the configuration the memory-bound GEMM takes on 128-144 SMs
     (256, 1792, 1032, 8, (224, 2)),
     # degenerate shapes: boxes far larger than the tensor on one or both sides
     (1, 1, 8, 0, None),                # a single output (scalar store path)
@@ -84,12 +84,16 @@ def test_gemm_full_size_memory_bound_every_entry(c3):
     # The bench workload in the bench's launch configuration: 256 x 28672 x 8192,
     # N(0,1) activations, N(0,0.02) weights, every SM.  Every one of the 7.3 M
     # outputs is checked against the oracle (fp64, multi-threaded on the host).
+    # The same shape on 144 SMs (a partition of 8 SMs to the collective) takes
+    # the 256 x 224 tile configuration in one wave: checked in full as well.
     w = I.WORKLOADS["mem_ag"]
     assert c3.c3_gemm_plan(w.M, w.N, w.K, 0)[:2] == (192, 2)
+    assert c3.c3_gemm_plan(w.M, w.N, w.K, 144)[:2] == (224, 2)
     A, B = I.gemm_operands(w)
-    C = run_gemm(c3, A, B, 0)
     C_ref, S_ref = oracle.gemm(A, B)
-    assert_gemm_close(C, C_ref, S_ref)
+    for budget in (0, 144):
+        C = run_gemm(c3, A, B, budget)
+        assert_gemm_close(C, C_ref, S_ref)
 
 
 def test_gemm_k_zero_writes_zeros(c3):
