@@ -73,9 +73,10 @@ __device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
 
 // Work unit of the vec kernel: 16 KiB (1024 16-byte vectors, four passes of
 // kVecUnroll vectors per lane) of one segment, moved by one warp.  Warp w of
-// the group's first launch part (w = CTA index in the group * 16 + warp) takes
-// unit w without asking; every other unit is claimed from the group's counter
-// (work[0]), numbered after those, so a warp that shares its SM with a GEMM
+// CTA b of the group's first launch part (F CTAs) takes unit w * F + b without
+// asking -- interleaved across CTAs, so that even a small collective spreads
+// over every SM of the part; every other unit is claimed from the group's
+// counter (work[0]), numbered after those, so a warp that shares its SM with a GEMM
 // CTA, or a CTA that starts late because its SM was busy, simply moves fewer
 // units.  Lane 0 claims the warp's next unit while the current one is copied
 // and broadcasts it by shuffle.  Within a pass every lane issues kVecUnroll
@@ -95,9 +96,11 @@ __global__ void __launch_bounds__(kVecThreads, 2)
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
     const uint64_t units_per_seg = (vecs_per_seg + kVecUnit - 1) / kVecUnit;
     const uint64_t total_units = units_per_seg * (uint64_t)t.nseg;
-    const unsigned gwarp = ((unsigned)cta_base + blockIdx.x) * kVecWarps + (threadIdx.x >> 5);
-    unsigned c = gwarp;
-    if (gwarp >= static_units) {
+    const unsigned cta = (unsigned)cta_base + blockIdx.x;
+    const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
+    const bool fixed_first = cta < first_ctas;
+    unsigned c = (threadIdx.x >> 5) * first_ctas + cta;
+    if (!fixed_first) {
         if (lane == 0) c = static_units + atomicAdd(&work[0], 1u);
         c = __shfl_sync(0xffffffffu, c, 0);
     }
@@ -175,14 +178,16 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             dst = t.dst[seg] + off;
         };
         // Claims the next chunk and issues its load into buffer issued % kBulkBufs.
-        // A CTA of the group's first launch part takes chunks b * kBulkBufs ..
-        // b * kBulkBufs + kBulkBufs - 1 (b its index in the group) without
-        // asking; every other chunk comes from the counter, numbered after those.
-        const uint32_t first = ((unsigned)cta_base + blockIdx.x) * (uint32_t)kBulkBufs;
+        // CTA b of the group's first launch part (F CTAs) takes chunks
+        // i * F + b, i = 0 .. kBulkBufs-1, without asking (interleaved, so a
+        // small collective still spreads over every SM of the part); every other
+        // chunk comes from the counter, numbered after those.
+        const uint32_t cta = (unsigned)cta_base + blockIdx.x;
+        const uint32_t first_ctas = static_units / (uint32_t)kBulkBufs;
         auto try_issue = [&]() {
             if (exhausted) return;
-            const uint32_t c = (first < static_units && issued < (uint32_t)kBulkBufs)
-                                   ? first + issued
+            const uint32_t c = (cta < first_ctas && issued < (uint32_t)kBulkBufs)
+                                   ? issued * first_ctas + cta
                                    : static_units + atomicAdd(&work[0], 1u);
             if (c >= total) {
                 exhausted = true;
