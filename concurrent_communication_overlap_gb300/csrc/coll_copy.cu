@@ -71,19 +71,20 @@ __device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
     }
 }
 
-// Work unit of the vec kernel: 16 KiB (1024 16-byte vectors, four passes of
-// kVecUnroll vectors per lane) of one segment, moved by one warp.  Warp w of
-// CTA b of the group's first launch part (F CTAs) takes unit w * F + b without
-// asking -- interleaved across CTAs, so that even a small collective spreads
-// over every SM of the part; every other unit is claimed from the group's
-// counter (work[0]), numbered after those, so a warp that shares its SM with a GEMM
-// CTA, or a CTA that starts late because its SM was busy, simply moves fewer
-// units.  Lane 0 claims the warp's next unit while the current one is copied
-// and broadcasts it by shuffle.  Within a pass every lane issues kVecUnroll
-// loads (each 512 contiguous bytes across the warp) before its stores.  The
-// kernel uses no shared memory, so it still fits beside a GEMM CTA.  A CTA none
-// of whose warps found work leaves at once and records no residency.
-constexpr uint64_t kVecUnit = 1024;  // vectors per unit (16 KiB)
+// Work of the vec kernel, in 4 KiB pieces of one segment (kVecUnroll 16-byte
+// vectors per lane of a warp: every lane issues its kVecUnroll loads, each 512
+// contiguous bytes across the warp, before its stores).  Warp w of CTA b of the
+// group's first launch part (F CTAs) moves piece w * F + b without asking --
+// interleaved across CTAs, so even a small collective spreads over every SM
+// of the part, each warp one round trip.  The pieces after those 16 F are
+// claimed from the group's counter (work[0]) four at a time (16 KiB), so a
+// warp that shares its SM with a GEMM CTA, or a CTA that starts late because
+// its SM was busy, simply moves fewer.  Lane 0 claims the warp's next four
+// while the current four are copied and broadcasts the claim by shuffle.  The
+// kernel uses no shared memory, so it still fits beside a GEMM CTA.  A CTA
+// none of whose warps found work leaves at once and records no residency.
+constexpr uint64_t kVecPiece = 32 * kVecUnroll;  // vectors per piece (4 KiB)
+constexpr unsigned kVecClaim = 4;                // pieces per claim
 constexpr int kVecWarps = kVecThreads / 32;
 
 template <bool kStream>
@@ -94,49 +95,60 @@ __global__ void __launch_bounds__(kVecThreads, 2)
     const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
-    const uint64_t units_per_seg = (vecs_per_seg + kVecUnit - 1) / kVecUnit;
-    const uint64_t total_units = units_per_seg * (uint64_t)t.nseg;
-    const unsigned cta = (unsigned)cta_base + blockIdx.x;
-    const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
-    const bool fixed_first = cta < first_ctas;
-    unsigned c = (threadIdx.x >> 5) * first_ctas + cta;
-    if (!fixed_first) {
-        if (lane == 0) c = static_units + atomicAdd(&work[0], 1u);
-        c = __shfl_sync(0xffffffffu, c, 0);
-    }
-    const bool worked = c < total_units;
-    while (c < total_units) {
-        unsigned next = 0;
-        if (lane == 0) next = static_units + atomicAdd(&work[0], 1u);
-        const uint64_t seg = c / units_per_seg;
-        const uint64_t vbase = (c - seg * units_per_seg) * kVecUnit;
+    const uint64_t pieces_per_seg = (vecs_per_seg + kVecPiece - 1) / kVecPiece;
+    const uint64_t total = pieces_per_seg * (uint64_t)t.nseg;
+    auto copy_piece = [&](uint64_t p) {
+        const uint64_t seg = p / pieces_per_seg;
+        const uint64_t vbase = (p - seg * pieces_per_seg) * kVecPiece + (uint64_t)lane;
         const uint8_t* src = t.src[seg];
         uint8_t* dst = t.dst[seg];
-#pragma unroll 1
-        for (uint64_t j = 0; j < kVecUnit; j += 32 * kVecUnroll) {
-            uint4 v[kVecUnroll];
+        uint4 v[kVecUnroll];
 #pragma unroll
-            for (int u = 0; u < kVecUnroll; ++u) {
-                const uint64_t i = vbase + j + (uint64_t)(u * 32 + lane);
-                if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
-            }
+        for (int u = 0; u < kVecUnroll; ++u) {
+            const uint64_t i = vbase + (uint64_t)(u * 32);
+            if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
+        }
 #pragma unroll
-            for (int u = 0; u < kVecUnroll; ++u) {
-                const uint64_t i = vbase + j + (uint64_t)(u * 32 + lane);
-                if (i < vecs_per_seg) {
-                    if (kStream)
-                        st_vec_stream(dst + (i << 4), v[u], pol);
-                    else
-                        st_vec(dst + (i << 4), v[u]);
-                }
+        for (int u = 0; u < kVecUnroll; ++u) {
+            const uint64_t i = vbase + (uint64_t)(u * 32);
+            if (i < vecs_per_seg) {
+                if (kStream)
+                    st_vec_stream(dst + (i << 4), v[u], pol);
+                else
+                    st_vec(dst + (i << 4), v[u]);
             }
         }
-        c = __shfl_sync(0xffffffffu, next, 0);
+    };
+    const unsigned cta = (unsigned)cta_base + blockIdx.x;
+    const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
+    bool worked = false;
+    if (cta < first_ctas) {
+        const uint64_t p = (uint64_t)(threadIdx.x >> 5) * first_ctas + cta;
+        if (p < total) {
+            copy_piece(p);
+            worked = true;
+        }
     }
-    // a hardware barrier reduction: did any warp of this CTA move a unit?
+    // pieces static_units + 4c .. static_units + 4c + 3 belong to claim c (none
+    // to claim when the fixed pieces cover the whole collective)
+    unsigned c = 0;
+    if (lane == 0 && (uint64_t)static_units < total) c = atomicAdd(&work[0], 1u);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    uint64_t p0 = (uint64_t)static_units < total ? (uint64_t)static_units + (uint64_t)c * kVecClaim : total;
+    while (p0 < total) {
+        worked = true;
+        unsigned next = 0;
+        if (lane == 0) next = atomicAdd(&work[0], 1u);
+#pragma unroll 1
+        for (unsigned q = 0; q < kVecClaim; ++q)
+            if (p0 + q < total) copy_piece(p0 + q);
+        c = __shfl_sync(0xffffffffu, next, 0);
+        p0 = (uint64_t)static_units + (uint64_t)c * kVecClaim;
+    }
+    // a hardware barrier reduction: did any warp of this CTA move a piece?
     const int cta_worked = __syncthreads_or(worked ? 1 : 0);
     if (threadIdx.x == 0) {
-        if (cta_worked) stamp_window(st, false, (unsigned)cta_base + blockIdx.x, t_enter, globaltimer());
+        if (cta_worked) stamp_window(st, false, cta, t_enter, globaltimer());
         group_done(work, total_ctas);
     }
 }
@@ -186,9 +198,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         const uint32_t first_ctas = static_units / (uint32_t)kBulkBufs;
         auto try_issue = [&]() {
             if (exhausted) return;
-            const uint32_t c = (cta < first_ctas && issued < (uint32_t)kBulkBufs)
-                                   ? issued * first_ctas + cta
-                                   : static_units + atomicAdd(&work[0], 1u);
+            const bool fixed = cta < first_ctas && issued < (uint32_t)kBulkBufs;
+            if (!fixed && (uint64_t)static_units >= total) {  // the fixed chunks cover everything
+                exhausted = true;
+                return;
+            }
+            const uint32_t c = fixed ? issued * first_ctas + cta : static_units + atomicAdd(&work[0], 1u);
             if (c >= total) {
                 exhausted = true;
                 return;
@@ -328,9 +343,9 @@ static uint64_t copy_units(const SegTable& t, uint64_t unit_bytes) {
 }
 
 bool copy_units_fit(const SegTable& t) {
-    // 32 KiB chunks are the smaller unit; keep the count (plus one overshooting
-    // claim per CTA) well inside 32 bits
-    return copy_units(t, kBulkChunk) < (1ull << 31);
+    // claims of 16 KiB (vec) and 32 KiB (bulk) counted in 32 bits: keep the
+    // count, plus one overshooting claim per warp, well inside that
+    return copy_units(t, 16 * 1024) < (1ull << 31);
 }
 
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
@@ -340,7 +355,7 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
     if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas || g.static_ctas < 0 ||
         g.static_ctas > g.total_ctas || (cta_base > 0 && cta_base < g.static_ctas))
         return set_error(-1, "copy launch group does not cover this launch");
-    if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 32 KiB chunks");
+    if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 16 KiB units");
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) return set_error(-1, "copy launch needs at least one CTA");
     // the group's first part (its first g.static_ctas CTAs) starts on fixed units
