@@ -73,16 +73,19 @@ __device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
 
 // Work of the vec kernel, in 4 KiB pieces of one segment (kVecUnroll 16-byte
 // vectors per lane of a warp: every lane issues its kVecUnroll loads, each 512
-// contiguous bytes across the warp, before its stores).  Warp w of CTA b of the
-// group's first launch part (F CTAs) moves piece w * F + b without asking --
-// interleaved across CTAs, so even a small collective spreads over every SM
-// of the part, each warp one round trip.  The pieces after those 16 F are
-// claimed from the group's counter (work[0]) four at a time (16 KiB), so a
-// warp that shares its SM with a GEMM CTA, or a CTA that starts late because
-// its SM was busy, simply moves fewer.  Lane 0 claims the warp's next four
-// while the current four are copied and broadcasts the claim by shuffle.  The
-// kernel uses no shared memory, so it still fits beside a GEMM CTA.  A CTA
-// none of whose warps found work leaves at once and records no residency.
+// contiguous bytes across the warp, before its stores).  The group's first
+// launch part (F CTAs of 16 warps) starts on fixed pieces, in up to four rounds
+// of 16 F: in round j, warp w of CTA b moves piece j * 16F + w * F + b --
+// interleaved across CTAs, so even a small collective spreads over every SM of
+// the part -- with as many rounds as the collective fills (one for a
+// collective of at most 16F pieces, four for a large one).  The pieces after
+// the fixed rounds are claimed from the group's counter (work[0]) four at a
+// time (16 KiB), so a warp that shares its SM with a GEMM CTA, or a CTA that
+// starts late because its SM was busy, simply moves fewer.  Lane 0 claims the
+// warp's next four while the current four are copied and broadcasts the claim
+// by shuffle.  The kernel uses no shared memory, so it still fits beside a
+// GEMM CTA.  A CTA none of whose warps found work leaves at once and records
+// no residency.
 constexpr uint64_t kVecPiece = 32 * kVecUnroll;  // vectors per piece (4 KiB)
 constexpr unsigned kVecClaim = 4;                // pieces per claim
 constexpr int kVecWarps = kVecThreads / 32;
@@ -121,20 +124,28 @@ __global__ void __launch_bounds__(kVecThreads, 2)
     };
     const unsigned cta = (unsigned)cta_base + blockIdx.x;
     const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
+    const uint64_t round = static_units;                     // 16 F pieces per fixed round
+    const uint64_t rounds = round ? (total + round - 1) / round < kVecClaim ? (total + round - 1) / round
+                                                                               : kVecClaim
+                                  : 0;
+    const uint64_t fixed = rounds * round;  // pieces 0 .. fixed-1 are dealt without the counter
     bool worked = false;
     if (cta < first_ctas) {
-        const uint64_t p = (uint64_t)(threadIdx.x >> 5) * first_ctas + cta;
-        if (p < total) {
-            copy_piece(p);
-            worked = true;
+#pragma unroll 1
+        for (uint64_t j = 0; j < rounds; ++j) {
+            const uint64_t p = j * round + (uint64_t)(threadIdx.x >> 5) * first_ctas + cta;
+            if (p < total) {
+                copy_piece(p);
+                worked = true;
+            }
         }
     }
-    // pieces static_units + 4c .. static_units + 4c + 3 belong to claim c (none
-    // to claim when the fixed pieces cover the whole collective)
+    // pieces fixed + 4c .. fixed + 4c + 3 belong to claim c (none to claim when
+    // the fixed rounds cover the whole collective)
     unsigned c = 0;
-    if (lane == 0 && (uint64_t)static_units < total) c = atomicAdd(&work[0], 1u);
+    if (lane == 0 && fixed < total) c = atomicAdd(&work[0], 1u);
     c = __shfl_sync(0xffffffffu, c, 0);
-    uint64_t p0 = (uint64_t)static_units < total ? (uint64_t)static_units + (uint64_t)c * kVecClaim : total;
+    uint64_t p0 = fixed < total ? fixed + (uint64_t)c * kVecClaim : total;
     while (p0 < total) {
         worked = true;
         unsigned next = 0;
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         for (unsigned q = 0; q < kVecClaim; ++q)
             if (p0 + q < total) copy_piece(p0 + q);
         c = __shfl_sync(0xffffffffu, next, 0);
-        p0 = (uint64_t)static_units + (uint64_t)c * kVecClaim;
+        p0 = fixed + (uint64_t)c * kVecClaim;
     }
     // a hardware barrier reduction: did any warp of this CTA move a piece?
     const int cta_worked = __syncthreads_or(worked ? 1 : 0);
