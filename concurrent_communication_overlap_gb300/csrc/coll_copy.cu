@@ -98,29 +98,41 @@ __global__ void __launch_bounds__(kVecThreads, 2)
     const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
-    const uint64_t pieces_per_seg = (vecs_per_seg + kVecPiece - 1) / kVecPiece;
-    const uint64_t total = pieces_per_seg * (uint64_t)t.nseg;
-    auto copy_piece = [&](uint64_t p) {
-        const uint64_t seg = p / pieces_per_seg;
-        const uint64_t vbase = (p - seg * pieces_per_seg) * kVecPiece + (uint64_t)lane;
-        const uint8_t* src = t.src[seg];
-        uint8_t* dst = t.dst[seg];
+    // piece counts fit in 32 bits (copy_units_fit bounds the collective)
+    const uint32_t pieces_per_seg = (uint32_t)((vecs_per_seg + kVecPiece - 1) / kVecPiece);
+    const uint64_t total = (uint64_t)pieces_per_seg * (uint64_t)t.nseg;
+    auto copy_piece = [&](uint32_t p) {
+        const uint32_t seg = p / pieces_per_seg;
+        const uint64_t vbase = (uint64_t)(p - seg * pieces_per_seg) * kVecPiece;
+        const uint8_t* src = t.src[seg] + ((vbase + (uint64_t)lane) << 4);
+        uint8_t* dst = t.dst[seg] + ((vbase + (uint64_t)lane) << 4);
         uint4 v[kVecUnroll];
+        if (vbase + kVecPiece <= vecs_per_seg) {
+            // a whole piece: 8 loads at fixed 512-byte strides from one base, then 8 stores
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const uint64_t i = vbase + (uint64_t)(u * 32);
-            if (i < vecs_per_seg) v[u] = kStream ? ld_vec_stream(src + (i << 4), pol) : ld_vec(src + (i << 4));
-        }
+            for (int u = 0; u < kVecUnroll; ++u) v[u] = kStream ? ld_vec_stream(src + u * 512, pol) : ld_vec(src + u * 512);
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const uint64_t i = vbase + (uint64_t)(u * 32);
-            if (i < vecs_per_seg) {
+            for (int u = 0; u < kVecUnroll; ++u) {
                 if (kStream)
-                    st_vec_stream(dst + (i << 4), v[u], pol);
+                    st_vec_stream(dst + u * 512, v[u], pol);
                 else
-                    st_vec(dst + (i << 4), v[u]);
+                    st_vec(dst + u * 512, v[u]);
             }
+            return;
         }
+        // the segment's ragged last piece
+#pragma unroll
+        for (int u = 0; u < kVecUnroll; ++u)
+            if (vbase + (uint64_t)(u * 32 + lane) < vecs_per_seg)
+                v[u] = kStream ? ld_vec_stream(src + u * 512, pol) : ld_vec(src + u * 512);
+#pragma unroll
+        for (int u = 0; u < kVecUnroll; ++u)
+            if (vbase + (uint64_t)(u * 32 + lane) < vecs_per_seg) {
+                if (kStream)
+                    st_vec_stream(dst + u * 512, v[u], pol);
+                else
+                    st_vec(dst + u * 512, v[u]);
+            }
     };
     const unsigned cta = (unsigned)cta_base + blockIdx.x;
     const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
@@ -135,7 +147,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         for (uint64_t j = 0; j < rounds; ++j) {
             const uint64_t p = j * round + (uint64_t)(threadIdx.x >> 5) * first_ctas + cta;
             if (p < total) {
-                copy_piece(p);
+                copy_piece((uint32_t)p);
                 worked = true;
             }
         }
@@ -152,7 +164,7 @@ __global__ void __launch_bounds__(kVecThreads, 2)
         if (lane == 0) next = atomicAdd(&work[0], 1u);
 #pragma unroll 1
         for (unsigned q = 0; q < kVecClaim; ++q)
-            if (p0 + q < total) copy_piece(p0 + q);
+            if (p0 + q < total) copy_piece((uint32_t)(p0 + q));
         c = __shfl_sync(0xffffffffu, next, 0);
         p0 = fixed + (uint64_t)c * kVecClaim;
     }
@@ -354,9 +366,9 @@ static uint64_t copy_units(const SegTable& t, uint64_t unit_bytes) {
 }
 
 bool copy_units_fit(const SegTable& t) {
-    // claims of 16 KiB (vec) and 32 KiB (bulk) counted in 32 bits: keep the
-    // count, plus one overshooting claim per warp, well inside that
-    return copy_units(t, 16 * 1024) < (1ull << 31);
+    // 4 KiB pieces (vec) and 32 KiB chunks (bulk) are numbered in 32 bits: keep
+    // the piece count, plus the overshooting claims, well inside that
+    return copy_units(t, 4 * 1024) < (1ull << 31);
 }
 
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
@@ -366,7 +378,7 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
     if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas || g.static_ctas < 0 ||
         g.static_ctas > g.total_ctas || (cta_base > 0 && cta_base < g.static_ctas))
         return set_error(-1, "copy launch group does not cover this launch");
-    if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 16 KiB units");
+    if (!copy_units_fit(t)) return set_error(-5, "collective has more than 2^31 4 KiB pieces");
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) return set_error(-1, "copy launch needs at least one CTA");
     // the group's first part (its first g.static_ctas CTAs) starts on fixed units
