@@ -34,9 +34,11 @@
  *   - Streams are `cudaStream_t` values passed as `c3_stream` (void *); NULL
  *     means the legacy default stream.
  *   - The library owns a few internal objects per device, created on first use
- *     with that device current and released by c3_shutdown(): three CUDA
- *     streams (the forked collective's, the same at the highest priority, and
- *     a private stream for capturing memcpy graphs), CUDA events, up to 16
+ *     with that device current and released by c3_shutdown(): four CUDA
+ *     streams (the forked collective's, the same at the highest priority, a
+ *     second collective stream for the part of a partitioned collective that
+ *     waits for the GEMM's SMs, and a private stream for capturing memcpy
+ *     graphs), CUDA events, up to 16
  *     cached memcpy graphs, a 16 KiB device status block
  *     (error word, %globaltimer stamps, per-CTA %smid residency records) and
  *     the kernels' function attributes.
