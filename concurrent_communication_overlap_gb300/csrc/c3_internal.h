@@ -23,7 +23,8 @@ constexpr int kSchedSlots = 64;    // GEMM tile-scheduler counters, used round-r
 struct DevStatus {
     int error;                     // 0, or a negative c3_status (first writer wins)
     int where;                     // code of the wait that gave up
-    int pad0, pad1;
+    unsigned int gemm_started;     // GEMM CTAs that have started since the last reset
+    int pad1;
     unsigned long long gemm_t0;    // min CTA start of the GEMM (%globaltimer, ns)
     unsigned long long gemm_t1;    // max CTA end
     unsigned long long comm_t0;    // same for the SM collective
@@ -157,8 +158,11 @@ struct CopyGroup {
 // Picks the next work-counter slot of the device (round robin) for a group of
 // total_ctas CTAs whose first launch part has first_ctas CTAs.
 CopyGroup copy_group(DeviceState& ds, int total_ctas, int first_ctas);
+// gate_need > 0: each CTA of this launch first reads st->gemm_started and, if
+// fewer than gate_need GEMM CTAs have started, leaves at once without work (it
+// was dispatched before a GEMM whose CTAs still wait for SMs).
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
-                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out);
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need = 0);
 // Largest number of work units (64 KiB rounds / 32 KiB chunks) a collective may
 // have: the 32-bit counters stay far from wrapping.
 bool copy_units_fit(const SegTable& t);

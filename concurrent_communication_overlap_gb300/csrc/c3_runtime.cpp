@@ -370,7 +370,7 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
 // widens to them once the GEMM's CTAs finish (a CTA that finds no work left
 // exits at once).  An all-reduce's copies wait for its reduce-scatter.
 static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, int l2_stream, int first, int rest,
-                            const CopyGroup& g, cudaStream_t s2, int* ctas) {
+                            const CopyGroup& g, cudaStream_t s2, int* ctas, unsigned gemm_ctas) {
     if (ctas) *ctas = 0;
     const SegTable& t = cp.seg;
     if (rest <= 0 || t.nseg == 0 || t.seg_bytes == 0) return 0;
@@ -380,7 +380,7 @@ static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, 
     }
     const int flavour = pick_flavour(t, sm_kernel, true);
     const int reserve = flavour == kSmkVec ? exclusive_reserve(ds) : 0;
-    return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas);
+    return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas, gemm_ctas);
 }
 
 // A split group whose second part could not be launched would never count to
@@ -585,8 +585,9 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         };
         auto go_rest = [&] {
             if (!part) return (int)C3_OK;
+            // gated on the GEMM: its CTAs leave at once while GEMM CTAs still wait for SMs
             int r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sc2,
-                                     &cctas2);
+                                     &cctas2, (unsigned)gctas);
             rest_launched = (r == C3_OK);
             if (r == C3_OK && (e = cudaEventRecord(ev_c2, sc2)) != cudaSuccess) r = set_cuda_error(e, "event record");
             return r;

@@ -18,6 +18,7 @@ __global__ void status_reset_kernel(DevStatus* st) {
     if (i == 0) {
         st->error = 0;
         st->where = 0;
+        st->gemm_started = 0;
         st->gemm_t0 = ~0ull;
         st->gemm_t1 = 0;
         st->comm_t0 = ~0ull;

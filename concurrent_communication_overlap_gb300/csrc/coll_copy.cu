@@ -61,6 +61,21 @@ __device__ __forceinline__ void st_vec_stream(uint8_t* p, uint4 v, uint64_t pol)
                  : "memory");
 }
 
+// The gate of a collective launch part that must start only on SMs a GEMM has
+// left: the hardware may dispatch that launch's CTAs before the GEMM's own
+// (both wait for the same free SMs), and such a CTA, holding its SM while the
+// GEMM still has CTAs waiting, would turn the run serial.  Every GEMM CTA adds
+// itself to st->gemm_started as it starts; a gated CTA that finds fewer than
+// gate_need started leaves at once, without work (one read, no waiting; a
+// stale read only makes it leave when it could have stayed).  The whole CTA
+// takes the same decision (one value, broadcast through a barrier reduction).
+__device__ __forceinline__ bool gate_closed(const DevStatus* st, unsigned gate_need) {
+    if (gate_need == 0 || st == nullptr) return false;
+    int closed = 0;
+    if (threadIdx.x == 0) closed = *reinterpret_cast<const volatile unsigned*>(&st->gemm_started) < gate_need;
+    return __syncthreads_or(closed) != 0;
+}
+
 // The last CTA of a launch group to finish puts the group's work counter back
 // to zero, so the slot is clean for its next user.
 __device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
@@ -93,8 +108,12 @@ constexpr int kVecWarps = kVecThreads / 32;
 template <bool kStream>
 __global__ void __launch_bounds__(kVecThreads, 2)
     copy_vec_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
-                    unsigned static_units) {
+                    unsigned static_units, unsigned gate_need) {
     const unsigned long long t_enter = globaltimer();
+    if (gate_closed(st, gate_need)) {
+        if (threadIdx.x == 0) group_done(work, total_ctas);
+        return;
+    }
     const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
     const uint64_t vecs_per_seg = t.seg_bytes >> 4;
@@ -184,7 +203,11 @@ __global__ void __launch_bounds__(kVecThreads, 2)
 template <bool kStream>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     copy_bulk_kernel(SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
-                     unsigned static_units) {
+                     unsigned static_units, unsigned gate_need) {
+    if (gate_closed(st, gate_need)) {
+        if (threadIdx.x == 0) group_done(work, total_ctas);
+        return;
+    }
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kBulkBufs];
     __shared__ int abort_flag;
@@ -372,7 +395,7 @@ bool copy_units_fit(const SegTable& t) {
 }
 
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
-                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out) {
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
     if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas || g.static_ctas < 0 ||
@@ -385,15 +408,15 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
     if (flavour == kSmkBulk) {
         const unsigned su = (unsigned)g.static_ctas * (unsigned)kBulkBufs;
         if (l2_stream)
-            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
+            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
         else
-            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
+            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
     } else {
         const unsigned su = (unsigned)g.static_ctas * (unsigned)kVecWarps;
         if (l2_stream)
-            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
+            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
         else
-            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su);
+            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "copy kernel launch");

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (threadIdx.x == 0) {
         stamp_begin(st, true);
+        if (st) atomicAdd(&st->gemm_started, 1u);  // read by collective CTAs that wait for the GEMM's SMs
         *abort_flag = 0;
         for (int i = 0; i < S; ++i) {
             mbar_init(bar(i), 1);
