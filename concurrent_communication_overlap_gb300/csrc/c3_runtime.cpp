@@ -547,9 +547,13 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // forked onto a stream of its own: one cross-stream dependency on
         // the way in and one on the way out, instead of two each.
         cudaStream_t sg = s0;
-        cudaStream_t sc = priority ? ds.s_comm_hi : ds.s_comm;
-        if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         const bool reclaim = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
+        // With reclaim the GEMM is launched on every SM, so the partition exists only
+        // if the collective's CTAs are dispatched first: its stream takes the highest
+        // priority, and the hardware hands pending CTAs of a higher-priority stream
+        // the free SMs first.
+        cudaStream_t sc = (priority || reclaim) ? ds.s_comm_hi : ds.s_comm;
+        if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
         if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
         // Partitioning (sm_split > 0 on SMs): the collective starts on sm_split
         // SMs it holds alone and the GEMM on the others (capped at SM count -

@@ -339,11 +339,17 @@ typedef struct {
  *     inside the driver on GB300; copies from page-locked host sources are DMA.)
  *   mode C3_MODE_CONCURRENT_SM_RECLAIM (sm_split >= 1): SM partitioning with
  *     reclaim -- the collective is launched first on sm_split SMs it holds
- *     alone, the GEMM on every SM; the GEMM CTAs that find no free SM start
- *     as soon as the collective's SMs free up and, since the GEMM claims its
- *     tiles dynamically, take only the tiles still left.  The partition lasts
- *     as long as the collective, not as long as the GEMM.  priority selects
- *     the collective's stream priority.
+ *     alone, on the library's highest-priority stream so that its CTAs are
+ *     dispatched before the GEMM's, the GEMM on every SM; the GEMM CTAs that
+ *     find no free SM start as soon as the collective's SMs free up and, since
+ *     the GEMM claims its tiles dynamically, take only the tiles still left.
+ *     The partition lasts as long as the collective, not as long as the GEMM.
+ *     priority has no further effect in this mode.
+ *   In both partitioned modes the collective is one launch group of SM-count
+ *   CTAs: its first sm_split CTAs as above, and the rest launched after the
+ *   GEMM on another library stream, gated on the GEMM (a CTA that starts while
+ *   GEMM CTAs still wait for SMs leaves at once), so they run only on SMs the
+ *   GEMM has left: a collective that outlasts the GEMM widens onto them.
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error

@@ -200,3 +200,24 @@ def test_partitioned_link_collective_overlaps_the_gemm(c3, mode, split):
         assert r["status"] == 0
         assert r["t_conc"] < 0.8 * (r["t_gemm_iso"] + r["t_comm_iso"]), r
     assert np.array_equal(out.cpu().numpy(), oracle.allgather(shards))
+
+
+@pytest.mark.parametrize("mode,split", [(4, 8), (4, 32)])
+def test_reclaim_link_collective_overlaps_the_compute_bound_ffn_gemm(c3, mode, split):
+    """The Llama-70B-FFN-shaped GEMM (2 ms) beside a 448 MiB all-gather from
+    host memory (link-bound, ~2.2 ms) with reclaim: the collective's first
+    part must hold its SMs from the start, beside the GEMM, not after it."""
+    M, N, K = 8192, 28672, 8192
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    dA = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+    dB = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    sb = 56 << 20
+    hs = [torch.randint(0, 256, (sb,), dtype=torch.uint8).pin_memory() for _ in range(8)]
+    out = torch.zeros(8 * sb, dtype=torch.uint8, device="cuda")
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLGATHER, out, sb, 8, shards=hs, settle_us=5000)
+    for r in c3.c3_time(p, mode, split, 0, warmup=1, reps=3):
+        assert r["status"] == 0
+        assert r["t_conc"] < 0.8 * (r["t_gemm_iso"] + r["t_comm_iso"]), r
+    assert torch.equal(out.cpu(), torch.cat(hs))
