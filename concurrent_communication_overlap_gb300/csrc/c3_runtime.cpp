@@ -517,22 +517,38 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     PhaseRange range(mode_range_name(mode, sm_split, priority));
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);
     cudaEvent_t ev0 = ds.ev[0], ev_g = ds.ev[1], ev_c = ds.ev[2], ev_end = ds.ev[3];
-    int rc = status_reset_launch(ds.status, s0);
-    if (rc) return rc;
+    const bool reclaim_mode = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
+    int rc = 0;
     cudaError_t e;
+    // With reclaim the GEMM is launched on every SM, so the collective's first
+    // part must reach the hardware first or the GEMM takes every SM.  The
+    // queue that records the start event is the one that proceeds first once
+    // earlier work (an L2 flush) drains -- another stream has to notice the
+    // event -- so in this mode the status reset, the start event and the
+    // collective's first part all go on the collective's stream, and the
+    // caller's stream waits for the start event before the GEMM.
+    cudaStream_t sc_first = nullptr;
+    if (reclaim_mode) {
+        sc_first = ds.s_comm_hi;
+        if ((e = cudaEventRecord(ds.ev[4], s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+        if ((e = cudaStreamWaitEvent(sc_first, ds.ev[4], 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        if ((rc = status_reset_launch(ds.status, sc_first))) return rc;
+    } else if ((rc = status_reset_launch(ds.status, s0))) {
+        return rc;
+    }
     int gctas = 0, cctas = 0;
     bool split_rest = false;  // the collective ran as a split launch group (second part on ds.ev[6])
     const bool serial = (mode == C3_MODE_SERIAL_SM || mode == C3_MODE_SERIAL_CE);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
     // Host-side GEMM planning (tile choice, tensor maps) happens before the
     // start event: only device work and launch calls are timed.
-    const bool reclaim_mode = (mode == C3_MODE_CONCURRENT_SM_RECLAIM);
     const int gemm_cap = (!serial && sm_split > 0 && !reclaim_mode) ? ds.sm_count - sm_split : 0;
     GemmLaunch gl;
     if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, gemm_cap, &gl))) return rc;
     // with reclaim, CTAs that find their SM held start late: every tile, the first included, is claimed
     if (reclaim_mode) gl.static_first = 0;
-    if ((e = cudaEventRecord(ev0, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
+    if ((e = cudaEventRecord(ev0, reclaim_mode ? sc_first : s0)) != cudaSuccess)
+        return set_cuda_error(e, "event record");
     if (serial) {
         rc = gemm_enqueue(gl, s0, ds.status, &gctas);
         if (rc) return rc;
@@ -553,7 +569,12 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // priority, and the hardware hands pending CTAs of a higher-priority stream
         // the free SMs first.
         cudaStream_t sc = (priority || reclaim) ? ds.s_comm_hi : ds.s_comm;
-        if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        if (reclaim) {
+            // sc already follows the start event in order; the GEMM's stream waits for it
+            if ((e = cudaStreamWaitEvent(s0, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
+        } else if ((e = cudaStreamWaitEvent(sc, ev0, 0)) != cudaSuccess) {
+            return set_cuda_error(e, "fork");
+        }
         if (reclaim && sm_split < 1) return set_error(C3_EINVAL, "the reclaim mode needs sm_split >= 1");
         // Partitioning (sm_split > 0 on SMs): the collective starts on sm_split
         // SMs it holds alone and the GEMM on the others (capped at SM count -
