@@ -78,8 +78,8 @@ MODES = [
 # prioritised launch and the partitions with reclaim (the GEMM takes the
 # collective's SMs back once it is done) ride along.
 DEFAULT_MODES = {
-    "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_8",
-                 "reclaim_16", "reclaim_32", "reclaim_64", "ce", "ce_rp_8"],
+    "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_16",
+                 "ce", "ce_rp_8"],
 }
 
 
