@@ -201,8 +201,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 unsigned next_raw = 0;
                 int mb, nb;
                 tile_coords(t, num_m, num_n, mb, nb);
+                // With a single row block every tile reads the same A panel.
+                // Each tile then walks K from its own starting block (spread
+                // evenly over the column blocks), so that at any moment the
+                // CTAs read different parts of A instead of all asking L2 for
+                // the same lines.  The accumulation order follows the loads.
+                int kx = (num_m == 1) ? (int)(((long long)nb * num_kb) / num_n) : 0;
                 bool ok = true;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; ++kb, kx = (kx + 1 == num_kb) ? 0 : kx + 1) {
                     if (!mbar_wait(bar(S + stage), phase ^ 1u, abort_flag)) {
                         report_error(st, -4, kSiteGemmProducer);
                         ok = false;
@@ -211,8 +217,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     mbar_arrive_expect_tx(bar(stage), Cfg::kStageBytes);
 #pragma unroll
                     for (int sub = 0; sub < MSUB; ++sub)
-                        tma_load_2d(stage_a(stage, sub), &tmA, bar(stage), kb * kBK, mb * kRowsCta + sub * kBM, pol_a);
-                    tma_load_2d(stage_b(stage), &tmB, bar(stage), kb * kBK, nb * BN, pol_b);
+                        tma_load_2d(stage_a(stage, sub), &tmA, bar(stage), kx * kBK, mb * kRowsCta + sub * kBM, pol_a);
+                    tma_load_2d(stage_b(stage), &tmB, bar(stage), kx * kBK, nb * BN, pol_b);
                     if (kb == 0 && sched) next_raw = atomicAdd(&sched[0], 1u);
                     if (++stage == S) {
                         stage = 0;
@@ -452,8 +458,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_arrive(bar(BAR_TEMPTY + buf));
             }
         }
-        // every TMA store this warp issued has completed before the CTA ends
-        if (lane == 0) bulk_wait_all();
+        // Every TMA store this warp issued has finished reading shared memory
+        // before the CTA ends; their writes to C are complete when the grid is.
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
     }
 
