@@ -98,7 +98,9 @@ def select_modes(workload, names=""):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: as many as fit in about a minute of timed work at the pace of "
+                         "the warm-up steps, 10 to 200; 5 per size for --sweep)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
@@ -467,6 +469,20 @@ def dist_init(args):
     return world, rank, local, pg
 
 
+STEP_BUDGET_S = 60.0
+AUTO_STEPS_MIN, AUTO_STEPS_MAX = 10, 200
+
+
+def auto_steps(per_step_s, budget_s=STEP_BUDGET_S, lo=AUTO_STEPS_MIN, hi=AUTO_STEPS_MAX):
+    """Timed steps when --steps is not given: as many as fit in budget_s of
+    timed work at the warm-up steps' pace, clamped to lo .. hi.  A long step
+    (the 8192x53248x16384 pair with its settle periods takes ~0.8 s) gets
+    fewer steps than a short one, and the timed region stays near a minute."""
+    if per_step_s <= 0.0:
+        return hi
+    return max(lo, min(hi, int(budget_s / per_step_s)))
+
+
 def reduce_max(pg, value, device=None):
     if pg is None:
         return value
@@ -570,6 +586,8 @@ def run_reference(args, world, rank, pg):
     t0 = time.perf_counter()
     # size the sample so that the whole run (3 oracle GEMM phases per step)
     # stays near a minute, whatever --steps asks for
+    if args.steps is None:
+        args.steps = AUTO_STEPS_MAX
     target = min(0.5, 60.0 / (3.0 * max(1, args.steps + args.warmup)))
     recs, sample, cores = cpu_c3(w, args.steps, args.warmup, target_s=target)
     wall = time.perf_counter() - t0
@@ -612,6 +630,8 @@ def run_sweep(args, c3, torch, np, I, dev, info):
         raise SystemExit("--sweep-max-mib must be a power of two")
     ws = I.sweep_workloads(args.sweep, hi_bytes=args.sweep_max_mib << 20)
     host_src = args.coll_src == "host"
+    if args.steps is None:
+        args.steps = 5
 
     def place(a):
         return place_source(torch, a, dev, host_src)
@@ -862,11 +882,15 @@ def main(argv=None):
         print(json.dumps({"profile_range": args.profile_range, "workload": w.name}), flush=True)
         return 0
 
-    # ---- warm-up steps
+    # ---- warm-up steps (their pace sizes the timed region when --steps is not given)
+    t_warm = time.perf_counter()
     for _ in range(args.warmup):
         for name, mode, split, prio in modes:
             c3.c3_time(prob, mode, split, prio, warmup=0, reps=1)
     torch.cuda.synchronize(dev)
+    if args.steps is None:
+        per_step_s = (time.perf_counter() - t_warm) / max(1, args.warmup) if args.warmup > 0 else 0.0
+        args.steps = auto_steps(reduce_max(pg, per_step_s, dev))
 
     # ---- timed steps
     per_mode = {m[0]: [] for m in modes}

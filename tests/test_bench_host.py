@@ -237,3 +237,15 @@ def test_collective_bound_of_the_strict_engine():
     assert bench.coll_bound_strict(per_mode, modes, {"sm": 1.01, "ce": 0.1}, 1) == "latency"
     assert bench.coll_bound_strict(per_mode, modes, {}, 1) == "unknown"
     assert bench.most_common(["a", "b", "b"]) == "b" and bench.most_common([]) is None
+
+
+def test_default_step_count_fits_about_a_minute_of_timed_work():
+    # the 8192x53248x16384 pair with its settle periods: ~0.8 s a step
+    assert bench.auto_steps(0.8) == 75
+    assert bench.auto_steps(0.8) * 0.8 <= bench.STEP_BUDGET_S
+    # short steps: capped, long steps: never below the floor
+    assert bench.auto_steps(0.01) == bench.AUTO_STEPS_MAX
+    assert bench.auto_steps(30.0) == bench.AUTO_STEPS_MIN
+    assert bench.auto_steps(0.0) == bench.AUTO_STEPS_MAX
+    assert bench.parse_args([]).steps is None
+    assert bench.parse_args(["--steps", "7"]).steps == 7
