@@ -70,7 +70,22 @@ MODES = [
     ("ce", 2, 0, 0),
     ("ce_rp_8", 2, 8, 0),
     ("ce_rp_16", 2, 16, 0),
+    ("ce_staged", 2, 0, 0),
 ]
+
+# Modes whose copy-engine collective is bounced through page-locked host
+# memory (C3_CE_HOST_STAGED): both hops are DMA, no SM moves a byte of it, at
+# the CPU-GPU link's rate.  They run on a problem record of their own (the one
+# carrying the bounce buffer) and count as an engine of their own.
+STAGED_MODES = {"ce_staged"}
+
+
+def mode_engine(name, mode):
+    """The engine a mode's collective runs on: 'sm', 'ce' (driver memcpy
+    between device buffers) or 'ce_staged' (DMA through host memory)."""
+    if name in STAGED_MODES:
+        return "ce_staged"
+    return "ce" if mode in (2, 3) else "sm"
 
 # Modes a workload runs by default (every mode otherwise).  The Llama-405B
 # pair names its own set: the copy kernel on every SM, on 8/16/32 SMs, and
@@ -79,7 +94,7 @@ MODES = [
 # collective's SMs back once it is done) ride along.
 DEFAULT_MODES = {
     "l405_a2a": ["baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "reclaim_16",
-                 "ce", "ce_rp_8"],
+                 "ce", "ce_rp_8", "ce_staged"],
 }
 
 
@@ -246,8 +261,7 @@ def coll_bound_strict(per_mode, modes, plateaus, coll_bytes):
     rate (the same rule as the library's c3_coll_bound)."""
     by_engine = {}
     for name, mode, split, prio in modes:
-        eng = "ce" if mode in (2, 3) else "sm"
-        by_engine.setdefault(eng, []).extend(r["t_comm_iso"] for r in per_mode[name])
+        by_engine.setdefault(mode_engine(name, mode), []).extend(r["t_comm_iso"] for r in per_mode[name])
     means = {e: step_mean(v) for e, v in by_engine.items() if v}
     if not means:
         return None
@@ -270,8 +284,7 @@ def strict_comm_time(per_mode, modes):
     engine): the strict T_comm for every mode's ideal."""
     by_engine = {}
     for name, mode, split, prio in modes:
-        eng = "ce" if mode in (2, 3) else "sm"
-        by_engine.setdefault(eng, []).extend(r["t_comm_iso"] for r in per_mode[name])
+        by_engine.setdefault(mode_engine(name, mode), []).extend(r["t_comm_iso"] for r in per_mode[name])
     return min(step_mean(v) for v in by_engine.values() if v)
 
 
@@ -625,7 +638,7 @@ def run_sweep(args, c3, torch, np, I, dev, info):
     per size."""
     names = (args.modes.split(",") if args.modes
              else ["baseline", "prioritised", "partitioned_32", "partitioned_64", "reclaim_16", "ce"])
-    modes = [m for m in MODES if m[0] in names]
+    modes = [m for m in MODES if m[0] in names and m[0] not in STAGED_MODES]
     if args.sweep_max_mib < 1 or args.sweep_max_mib & (args.sweep_max_mib - 1):
         raise SystemExit("--sweep-max-mib must be a power of two")
     ws = I.sweep_workloads(args.sweep, hi_bytes=args.sweep_max_mib << 20)
@@ -852,6 +865,19 @@ def main(argv=None):
                       ce_variant=ce_variant_arg(args, c3), settle_us=settle_us,
                       peak_flops=peaks["bf16_tflops"] * 1e12, peak_bytes_per_s=peaks["hbm_gbs"] * 1e9,
                       coll_plateau_sm=plateaus.get("sm", 0.0), coll_plateau_ce=plateaus.get("ce", 0.0))
+    # the host-staged modes: their own record, with a page-locked bounce buffer of the copies' size
+    # (sources in host memory reach the copy engines without one)
+    if host_src:
+        modes = [m for m in modes if m[0] not in STAGED_MODES]
+    probs = {m[0]: prob for m in modes}
+    if any(m[0] in STAGED_MODES for m in modes):
+        stage = torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory()
+        prob_staged = c3.Problem(dA, dB, dC, w.M, w.N, w.K, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
+                                 send=dsend, flush=flush, stream=stream, coll_l2=coll_l2_arg(args, c3),
+                                 ce_variant=c3.C3_CE_HOST_STAGED, settle_us=settle_us,
+                                 peak_flops=peaks["bf16_tflops"] * 1e12, peak_bytes_per_s=peaks["hbm_gbs"] * 1e9,
+                                 coll_plateau_sm=plateaus.get("sm", 0.0), ce_stage=stage)
+        probs.update({m[0]: prob_staged for m in modes if m[0] in STAGED_MODES})
 
     if args.profile_range:
         # one profiled phase on the real workload buffers, after a few untimed runs
@@ -886,7 +912,7 @@ def main(argv=None):
     t_warm = time.perf_counter()
     for _ in range(args.warmup):
         for name, mode, split, prio in modes:
-            c3.c3_time(prob, mode, split, prio, warmup=0, reps=1)
+            c3.c3_time(probs[name], mode, split, prio, warmup=0, reps=1)
     torch.cuda.synchronize(dev)
     if args.steps is None:
         per_step_s = (time.perf_counter() - t_warm) / max(1, args.warmup) if args.warmup > 0 else 0.0
@@ -902,7 +928,7 @@ def main(argv=None):
         ev0.record(stream)
         for _ in range(args.steps):
             for name, mode, split, prio in modes:
-                per_mode[name].extend(c3.c3_time(prob, mode, split, prio, warmup=0, reps=1))
+                per_mode[name].extend(c3.c3_time(probs[name], mode, split, prio, warmup=0, reps=1))
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(pg, dev)
@@ -928,7 +954,7 @@ def main(argv=None):
     for name, mode, split, prio in modes:
         out.fill_(0xA5)
         dC.fill_(float("nan"))
-        c3.c3_run(prob, mode, split, prio)
+        c3.c3_run(probs[name], mode, split, prio)
         per_mode_ok[name] = outputs_ok()
     torch.cuda.synchronize(dev)
 

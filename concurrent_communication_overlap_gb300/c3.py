@@ -23,7 +23,7 @@ C3_MODE_SERIAL_SM, C3_MODE_CONCURRENT_SM, C3_MODE_CONCURRENT_CE, C3_MODE_SERIAL_
 C3_MODE_CONCURRENT_SM_RECLAIM = 4
 C3_SMK_AUTO, C3_SMK_VEC, C3_SMK_BULK = 0, 1, 2
 C3_L2_NORMAL, C3_L2_EVICT_FIRST = 0, 1
-C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH, C3_CE_GRAPH_PARALLEL = 0, 1, 2, 3
+C3_CE_PER_SEGMENT, C3_CE_STRIDED, C3_CE_GRAPH, C3_CE_GRAPH_PARALLEL, C3_CE_HOST_STAGED = 0, 1, 2, 3, 4
 C3_FAULT_NONE, C3_FAULT_GEMM_LAUNCH, C3_FAULT_SM_COLL_LAUNCH, C3_FAULT_MEMCPY, C3_FAULT_DEVICE_INIT = 0, 1, 2, 3, 4
 CLASS_NAMES = {0: "G-long", 1: "GC-equal", 2: "C-long"}
 
@@ -43,7 +43,8 @@ class C3Problem(ctypes.Structure):
                 ("ce_variant", _int),
                 ("flush_buf", _vp), ("flush_bytes", _sz), ("stream", _vp),
                 ("settle_us", _int), ("peak_flops", ctypes.c_double), ("peak_bytes_per_s", ctypes.c_double),
-                ("coll_plateau_sm", ctypes.c_double), ("coll_plateau_ce", ctypes.c_double)]
+                ("coll_plateau_sm", ctypes.c_double), ("coll_plateau_ce", ctypes.c_double),
+                ("ce_stage", _vp), ("ce_stage_bytes", _sz)]
 
 
 _TIMING_DOUBLES = ["t_gemm_iso", "t_comm_iso", "t_serial", "t_serial_meas", "t_conc", "t_ideal", "s_ideal",
@@ -279,16 +280,23 @@ class Problem:
     def __init__(self, A, B, C, M, N, K, coll, recv, unit_bytes, nranks=8, shards=None, send=None,
                  comm_sms=0, sm_kernel=C3_SMK_AUTO, flush=None, stream=None, coll_l2=C3_L2_NORMAL,
                  ce_variant=C3_CE_PER_SEGMENT, settle_us=0, peak_flops=0.0, peak_bytes_per_s=0.0,
-                 coll_plateau_sm=0.0, coll_plateau_ce=0.0):
+                 coll_plateau_sm=0.0, coll_plateau_ce=0.0, ce_stage=None):
         self._shard_arr = None
         if shards is not None:
             self._shard_arr = (_vp * len(shards))(*[_ptr(s) for s in shards])
         fb, fn = (None, 0) if flush is None else (_ptr(flush), flush.numel() * flush.element_size())
+        # the host-staged copy-engine variant's bounce buffer: a page-locked tensor or (address, bytes)
+        if ce_stage is None:
+            sb, sn = None, 0
+        elif isinstance(ce_stage, tuple):
+            sb, sn = ce_stage
+        else:
+            sb, sn = _ptr(ce_stage), ce_stage.numel() * ce_stage.element_size()
         self.rec = C3Problem(_ptr(A), _ptr(B), _ptr(C), int(M), int(N), int(K), int(coll),
                              self._shard_arr, _ptr(send), _ptr(recv), int(unit_bytes), int(nranks),
                              int(comm_sms), int(sm_kernel), int(coll_l2), int(ce_variant), fb, fn,
                              _stream(stream), int(settle_us), float(peak_flops), float(peak_bytes_per_s),
-                             float(coll_plateau_sm), float(coll_plateau_ce))
+                             float(coll_plateau_sm), float(coll_plateau_ce), sb, int(sn))
 
 
 def c3_run(problem: Problem, mode, sm_split=0, priority=0, check=True):

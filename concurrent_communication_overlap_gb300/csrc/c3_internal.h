@@ -79,7 +79,7 @@ struct SegTable {
     int host_src;   // 1: at least one source is page-locked host memory (src[] holds its device address)
 };
 
-enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2, kCeGraphParallel = 3 };
+enum { kCePerSegment = 0, kCeStrided = 1, kCeGraph = 2, kCeGraphParallel = 3, kCeHostStaged = 4 };
 
 // A collective as launched: an optional reduce-scatter pass on SMs (all-reduce
 // only) followed by the segment copies on the chosen engine.
@@ -87,6 +87,7 @@ struct CollPlan {
     SegTable seg;
     RsTable rs;
     bool has_rs = false;
+    uint8_t* stage = nullptr;  // page-locked host bounce buffer of the host-staged copy-engine variant
 };
 
 enum { kSmkVec = 1, kSmkBulk = 2 };
@@ -171,7 +172,10 @@ int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStre
                           int* ctas_out);
 int bulk_copy_smem_bytes();
 
-int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream);
+// `stage`: the page-locked host bounce buffer of kCeHostStaged (at least
+// nseg * seg_bytes bytes), ignored by the other variants.
+int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream,
+                   uint8_t* stage = nullptr);
 
 // One-shot host-side failure injection (c3_inject_fault): true, and disarmed,
 // when `site` is the armed site.  Site values are those of c3_fault_site.

@@ -348,7 +348,7 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
             if (e != cudaSuccess) return set_cuda_error(e, "event record");
         }
         if (t.nseg == 0) return 0;
-        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
+        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture, cp.stage);
         const int flavour = pick_flavour(t, sm_kernel, exclusive);
         const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
         CopyGroup g = copy_group(ds, total, k);
@@ -356,7 +356,7 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
         int dummy = 0;
         return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, &dummy);
     }
-    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture);
+    if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture, cp.stage);
     const int flavour = pick_flavour(t, sm_kernel, exclusive);
     const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
     CopyGroup g = copy_group(ds, total, k);
@@ -474,7 +474,7 @@ static int check_problem(const c3_problem* p, CollPlan* cp) {
     if (rc) return rc;
     if (p->sm_kernel < C3_SMK_AUTO || p->sm_kernel > C3_SMK_BULK) return set_error(C3_EINVAL, "bad sm_kernel");
     if (p->coll_l2 != C3_L2_NORMAL && p->coll_l2 != C3_L2_EVICT_FIRST) return set_error(C3_EINVAL, "bad coll_l2");
-    if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_GRAPH_PARALLEL)
+    if (p->ce_variant < C3_CE_PER_SEGMENT || p->ce_variant > C3_CE_HOST_STAGED)
         return set_error(C3_EINVAL, "bad ce_variant");
     if (p->comm_sms < 0) return set_error(C3_EINVAL, "negative comm_sms");
     if (p->settle_us < 0 || p->settle_us > 1000000) return set_error(C3_EINVAL, "settle_us must be 0 .. 1000000");
@@ -486,6 +486,28 @@ static int check_problem(const c3_problem* p, CollPlan* cp) {
                                                    : t->seg_bytes * (size_t)t->nseg;
     if (overlaps(p->C, (size_t)p->M * (size_t)p->N * 4, p->recv, cb))
         return set_error(C3_EINVAL, "C overlaps the collective's output");
+    cp->stage = nullptr;
+    if (p->ce_variant == C3_CE_HOST_STAGED) {
+        // the copies move nseg * seg_bytes bytes (an all-reduce: its all-gather half, cb)
+        if (!p->ce_stage) return set_error(C3_EINVAL, "C3_CE_HOST_STAGED needs a bounce buffer (ce_stage)");
+        if (!aligned16(p->ce_stage)) return set_error(C3_EALIGN, "ce_stage must be 16-byte aligned");
+        if (p->ce_stage_bytes < t->seg_bytes * (size_t)t->nseg)
+            return set_error(C3_EINVAL, "ce_stage is smaller than the collective's copies");
+        cp->stage = static_cast<uint8_t*>(p->ce_stage);
+    }
+    return C3_OK;
+}
+
+// The bounce buffer of the host-staged copy-engine variant must be page-locked
+// host memory (both of its hops are then DMA), and the collective's sources
+// device memory (page-locked host sources are DMA already, without a bounce).
+static int locate_stage(const CollPlan& cp) {
+    if (!cp.stage) return C3_OK;
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, cp.stage);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaPointerGetAttributes (ce_stage)");
+    if (a.type != cudaMemoryTypeHost) return set_error(C3_EINVAL, "ce_stage must be page-locked host memory");
+    if (cp.seg.host_src) return set_error(C3_EUNSUP, "C3_CE_HOST_STAGED needs device sources");
     return C3_OK;
 }
 
@@ -921,6 +943,7 @@ int c3_run(const c3_problem* p, int mode, int sm_split, int priority, c3_timing*
     if (!ds) return C3_ECUDA;
     if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
     if ((rc = locate_plan(*ds, &t))) return rc;
+    if ((rc = locate_stage(t))) return rc;
     if (t.seg.host_src && p->sm_kernel == C3_SMK_BULK)
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only");
     out->mode = mode;
@@ -943,6 +966,7 @@ int c3_time(const c3_problem* p, int mode, int sm_split, int priority, int warmu
     if (!ds) return C3_ECUDA;
     if (sm_split < 0 || sm_split >= ds->sm_count) return set_error(C3_EINVAL, "sm_split must be 0 .. SM count - 1");
     if ((rc = locate_plan(*ds, &t))) return rc;
+    if ((rc = locate_stage(t))) return rc;
     if (t.seg.host_src && p->sm_kernel == C3_SMK_BULK)
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only");
     cudaStream_t s0 = static_cast<cudaStream_t>(p->stream);

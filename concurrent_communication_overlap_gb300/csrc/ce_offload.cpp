@@ -31,6 +31,11 @@
 //                SM kernel alone for all-gathers of >= 128 MiB, but a
 //                concurrent GEMM runs much slower beside it, and so do later
 //                concurrent runs in the same process.  Opt-in.
+//   HOST_STAGED  each segment device -> page-locked host -> device, two DMA
+//                transfers per piece, as a cached graph (build_graph_staged).
+//                The one way on this driver to move a collective between two
+//                device buffers with copy engines and no SM: the pages' DMA
+//                offload, paid for with two crossings of the CPU-GPU link.
 #include "c3_internal.h"
 
 #include <cstring>
@@ -62,8 +67,9 @@ static int ce_strided(const SegTable& t, cudaStream_t s) {
 // Small cache of instantiated graphs, keyed by the exact segment table.
 struct GraphEntry {
     bool used = false;
-    bool parallel = false;
+    int variant = kCeGraph;  // kCeGraph, kCeGraphParallel or kCeHostStaged
     int device = -1;
+    uint8_t* stage = nullptr;
     SegTable key;
     cudaGraphExec_t exec = nullptr;
     unsigned long long stamp = 0;
@@ -152,13 +158,58 @@ static int build_graph_captured(const SegTable& t, cudaStream_t capture_stream, 
     return 0;
 }
 
-static int ce_graph(const SegTable& t, bool parallel, cudaStream_t s, cudaStream_t capture_stream) {
+// HOST_STAGED: piece k of segment i (at most kStagePiece bytes, at offset
+// off) is two nodes, src[i] + off -> stage + i * seg_bytes + off (device to
+// host) and back to dst[i] + off (host to device).  The device-to-host nodes
+// form one chain and the host-to-device nodes another, and each piece's
+// second node also waits for its first: the two directions, which have
+// engines of their own, run at the same time one piece apart.  Pieces grow
+// past kStagePiece only to keep the graph within kStageMaxPieces pieces.
+constexpr uint64_t kStagePiece = 16ull << 20;
+constexpr uint64_t kStageMaxPieces = 512;
+
+static int build_graph_staged(const SegTable& t, uint8_t* stage, cudaGraphExec_t* exec) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaGraphCreate(&graph, 0);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphCreate");
+    auto fail = [&](cudaError_t err, const char* what) {
+        cudaGraphDestroy(graph);
+        return set_cuda_error(err, what);
+    };
+    const uint64_t total = t.seg_bytes * (uint64_t)t.nseg;
+    uint64_t piece = kStagePiece;
+    if (total / piece + (uint64_t)t.nseg > kStageMaxPieces) piece = total / (kStageMaxPieces - (uint64_t)t.nseg) + 1;
+    piece = (piece + 15) & ~15ull;
+    cudaGraphNode_t prev_d2h = nullptr, prev_h2d = nullptr;
+    for (int i = 0; i < t.nseg; ++i)
+        for (uint64_t off = 0; off < t.seg_bytes; off += piece) {
+            const uint64_t n = (t.seg_bytes - off) < piece ? (t.seg_bytes - off) : piece;
+            uint8_t* host = stage + (uint64_t)i * t.seg_bytes + off;
+            cudaGraphNode_t d2h = nullptr, h2d = nullptr;
+            e = cudaGraphAddMemcpyNode1D(&d2h, graph, prev_d2h ? &prev_d2h : nullptr, prev_d2h ? 1 : 0, host,
+                                         t.src[i] + off, (size_t)n, cudaMemcpyDeviceToHost);
+            if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode1D (device to host)");
+            cudaGraphNode_t deps[2] = {d2h, prev_h2d};
+            e = cudaGraphAddMemcpyNode1D(&h2d, graph, deps, prev_h2d ? 2 : 1, t.dst[i] + off, host, (size_t)n,
+                                         cudaMemcpyHostToDevice);
+            if (e != cudaSuccess) return fail(e, "cudaGraphAddMemcpyNode1D (host to device)");
+            prev_d2h = d2h;
+            prev_h2d = h2d;
+        }
+    e = cudaGraphInstantiate(exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return set_cuda_error(e, "cudaGraphInstantiate");
+    return 0;
+}
+
+static int ce_graph(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream,
+                    uint8_t* stage = nullptr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_cuda_error(e, "cudaGetDevice");
     GraphEntry* hit = nullptr;
     for (auto& g : g_graphs)
-        if (g.used && g.device == dev && g.parallel == parallel && same_table(g.key, t)) hit = &g;
+        if (g.used && g.device == dev && g.variant == variant && g.stage == stage && same_table(g.key, t)) hit = &g;
     if (!hit) {
         GraphEntry* victim = &g_graphs[0];
         for (auto& g : g_graphs) {
@@ -170,11 +221,13 @@ static int ce_graph(const SegTable& t, bool parallel, cudaStream_t s, cudaStream
         }
         if (victim->used && victim->exec) cudaGraphExecDestroy(victim->exec);
         *victim = GraphEntry();
-        int rc = parallel ? build_graph_parallel(t, &victim->exec)
-                          : build_graph_captured(t, capture_stream, &victim->exec);
+        int rc = variant == kCeGraphParallel ? build_graph_parallel(t, &victim->exec)
+                 : variant == kCeHostStaged  ? build_graph_staged(t, stage, &victim->exec)
+                                             : build_graph_captured(t, capture_stream, &victim->exec);
         if (rc) return rc;
         victim->used = true;
-        victim->parallel = parallel;
+        victim->variant = variant;
+        victim->stage = stage;
         victim->device = dev;
         victim->key = t;
         hit = victim;
@@ -185,12 +238,15 @@ static int ce_graph(const SegTable& t, bool parallel, cudaStream_t s, cudaStream
     return 0;
 }
 
-int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream) {
+int copy_ce_launch(const SegTable& t, int variant, cudaStream_t s, cudaStream_t capture_stream, uint8_t* stage) {
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
     if (take_fault(kFaultMemcpy)) return set_error(-3, "injected failure: memcpy transfer");
     if (variant == kCeStrided) return ce_strided(t, s);
-    if (variant == kCeGraph) return ce_graph(t, false, s, capture_stream);
-    if (variant == kCeGraphParallel) return ce_graph(t, true, s, capture_stream);
+    if (variant == kCeGraph || variant == kCeGraphParallel) return ce_graph(t, variant, s, capture_stream);
+    if (variant == kCeHostStaged) {
+        if (!stage) return set_error(-1, "host-staged copies need a bounce buffer");
+        return ce_graph(t, variant, s, capture_stream, stage);
+    }
     return ce_per_segment(t, s);
 }
 

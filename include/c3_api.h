@@ -110,12 +110,24 @@ typedef enum { C3_L2_NORMAL = 0, C3_L2_EVICT_FIRST = 1 } c3_l2_policy;
  * far more than beside the other variants, and later concurrent runs in the
  * same process do too -- opt-in only.  The pages' DMA collectives lose to the
  * compute-unit library below 32 MB on launch and synchronisation cost (Figure
- * 9); STRIDED and GRAPH cut the number of host calls per collective. */
+ * 9); STRIDED and GRAPH cut the number of host calls per collective.
+ * HOST_STAGED: every segment goes device -> page-locked host -> device as
+ * two transfers per piece of at most 16 MiB (c3_problem.ce_stage holds the
+ * pieces in between), replayed from a cached CUDA graph: the device-to-host
+ * pieces form one chain, the host-to-device pieces another, and each piece's
+ * second transfer waits for its first, so the two directions run at the same
+ * time one piece apart.  Both hops are copy-engine DMA; no SM runs any part
+ * of the collective.  It costs twice the CPU-GPU link traffic of the
+ * collective's bytes and runs at the link's rate (on GB300 about 3.8 ms for
+ * 1 GiB, against 0.16 ms for the SM kernel), so it pays only where a GEMM is
+ * long enough to hide it.  Needs device sources (C3_EUNSUP for page-locked
+ * host sources, which the other variants already reach by DMA). */
 typedef enum {
     C3_CE_PER_SEGMENT = 0,
     C3_CE_STRIDED = 1,
     C3_CE_GRAPH = 2,
-    C3_CE_GRAPH_PARALLEL = 3
+    C3_CE_GRAPH_PARALLEL = 3,
+    C3_CE_HOST_STAGED = 4
 } c3_ce_variant;
 
 /* The taxonomy class of a C3 pair (paper Section III, 115% / 15% thresholds). */
@@ -285,6 +297,14 @@ typedef struct {
                                   per second: classifies the collective as latency- or
                                   bandwidth-bound (0 = unknown) */
     double coll_plateau_ce;    /* the same for the copy-engine (memcpy) collective */
+    /* Bounce buffer of C3_CE_HOST_STAGED: page-locked host memory (cudaHostAlloc or
+     * cudaHostRegister), caller-owned, 16-byte aligned, at least the bytes the collective's
+     * copies move (all-gather and all-to-all: the output's size; all-reduce: the output's
+     * size, its all-gather half).  Read only when ce_variant is C3_CE_HOST_STAGED; NULL, too
+     * small, misaligned or not page-locked is then C3_EINVAL (C3_EALIGN for alignment).  Its
+     * contents are scratch. */
+    void *ce_stage;
+    size_t ce_stage_bytes;
 } c3_problem;
 
 /* Times in seconds. */

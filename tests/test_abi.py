@@ -47,6 +47,7 @@ int main(void) {
   F(c3_problem, coll); F(c3_problem, shards); F(c3_problem, unit_bytes); F(c3_problem, nranks);
   F(c3_problem, sm_kernel); F(c3_problem, flush_buf); F(c3_problem, stream);
   F(c3_problem, settle_us); F(c3_problem, peak_flops); F(c3_problem, coll_plateau_ce);
+  F(c3_problem, ce_stage); F(c3_problem, ce_stage_bytes);
   F(c3_timing, t_comm_ev); F(c3_timing, cls); F(c3_timing, smid_overlap); F(c3_timing, status);
   F(c3_timing, gemm_bound); F(c3_timing, coll_bound);
   F(c3_device_info, comm_default_sms);
@@ -143,6 +144,16 @@ def test_run_and_time_reject_bad_records(c3):
                        shards=[0x10000 * (r + 1) for r in range(8)], **kw)
         assert c3.lib().c3_time(ctypes.byref(q.rec), 1, 0, 0, 0, 1, arr) == c3.C3_EINVAL, kw
         assert c3.lib().c3_run(ctypes.byref(q.rec), 1, 0, 0, ctypes.byref(t)) == c3.C3_EINVAL, kw
+    # the host-staged copy-engine variant needs a 16-byte aligned bounce buffer of the copies' size
+    # (8 shards x 32 bytes here); an unknown variant is rejected
+    for kw, want in (({"ce_variant": 5}, c3.C3_EINVAL),
+                     ({"ce_variant": c3.C3_CE_HOST_STAGED}, c3.C3_EINVAL),
+                     ({"ce_variant": c3.C3_CE_HOST_STAGED, "ce_stage": (0x200000, 8 * 32 - 16)}, c3.C3_EINVAL),
+                     ({"ce_variant": c3.C3_CE_HOST_STAGED, "ce_stage": (0x200008, 8 * 32)}, c3.C3_EALIGN)):
+        q = c3.Problem(0x1000, 0x2000, 0x3000, 4, 4, 16, c3.C3_COLL_ALLGATHER, 0x100000, 32,
+                       shards=[0x10000 * (r + 1) for r in range(8)], **kw)
+        assert c3.lib().c3_run(ctypes.byref(q.rec), 2, 0, 0, ctypes.byref(t)) == want, kw
+        assert c3.lib().c3_time(ctypes.byref(q.rec), 2, 0, 0, 0, 1, arr) == want, kw
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):

@@ -190,7 +190,8 @@ def test_headline_line_keeps_every_mode_share_when_it_fits():
 
 def test_default_modes_of_the_405b_pair_and_explicit_subsets():
     names = [m[0] for m in bench.select_modes("l405_a2a")]
-    for n in ("baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "ce", "ce_rp_8"):
+    for n in ("baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "ce", "ce_rp_8",
+              "ce_staged"):
         assert n in names
     assert [m[0] for m in bench.select_modes("mem_ag")] == [m[0] for m in bench.MODES]
     assert [m[0] for m in bench.select_modes("l405_a2a", "ce,baseline")] == ["baseline", "ce"]
@@ -249,3 +250,19 @@ def test_default_step_count_fits_about_a_minute_of_timed_work():
     assert bench.auto_steps(0.0) == bench.AUTO_STEPS_MAX
     assert bench.parse_args([]).steps is None
     assert bench.parse_args(["--steps", "7"]).steps == 7
+
+
+def test_host_staged_mode_is_an_engine_of_its_own():
+    assert bench.mode_engine("ce_staged", 2) == "ce_staged"
+    assert bench.mode_engine("ce", 2) == "ce" and bench.mode_engine("ce_rp_8", 2) == "ce"
+    assert bench.mode_engine("baseline", 1) == "sm" and bench.mode_engine("reclaim_16", 4) == "sm"
+    # the strict T_comm is the fastest engine's mean: the staged DMA path's slow isolated time
+    # neither sets it nor blends into the driver memcpy's mean
+    modes = [("baseline", 1, 0, 0), ("ce", 2, 0, 0), ("ce_staged", 2, 0, 0)]
+    per_mode = {"baseline": [{"t_comm_iso": 2e-4}, {"t_comm_iso": 2e-4}],
+                "ce": [{"t_comm_iso": 3e-4}],
+                "ce_staged": [{"t_comm_iso": 3.8e-3}]}
+    assert bench.strict_comm_time(per_mode, modes) == pytest.approx(2e-4)
+    per_mode["baseline"] = [{"t_comm_iso": 5e-4}]
+    assert bench.strict_comm_time(per_mode, modes) == pytest.approx(3e-4)
+    assert bench.coll_bound_strict(per_mode, modes, {"ce": 1e12}, 1e8) == "latency"

@@ -4,6 +4,8 @@ collective is compared byte for byte with the oracle and the GEMM with the
 oracle's tolerance (pith.science verdict, skeptic critique "concrete_test").
 Also: the partitioned modes really run on disjoint SMs (%smid maps), and the
 timer's derived fields obey their definitions."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -251,3 +253,68 @@ def test_cta_windows_describe_the_last_run(c3, setup):
     cw = c3.c3_cta_windows(1)
     assert 1 <= len(cw) <= t["comm_ctas"]
     assert all(t0 <= t1 for _, _, t0, t1 in cw)
+
+
+@pytest.mark.parametrize("wname", ["tiny_ag", "tiny_a2a"])
+@pytest.mark.parametrize("mode,split", [(2, 0), (2, 8), (3, 0)])
+def test_host_staged_copy_engine_is_exact(c3, wname, mode, split):
+    """The copy-engine collective bounced through page-locked host memory
+    (C3_CE_HOST_STAGED: device -> host -> device in pieces of at most 16 MiB,
+    two DMA chains) delivers the oracle's bytes, concurrently with the GEMM
+    and serially, and runs no collective kernel of this library."""
+    s = Setup(c3, wname)
+    w = s.w
+    stage = torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory()
+    stage.fill_(0x5A)
+    p = c3.Problem(s.dA, s.dB, s.dC, w.M, w.N, w.K, s.p.rec.coll, s.out, w.unit_bytes, w.nranks,
+                   shards=s.dshards, send=s.dsend, flush=s.flush, ce_variant=c3.C3_CE_HOST_STAGED, ce_stage=stage)
+    for _ in range(2):  # the second run replays the cached graph
+        s.poison()
+        t = c3.c3_run(p, mode, split, 0)
+        assert t["status"] == 0 and t["comm_ctas"] == 0
+        s.verify()
+    # the bounce buffer holds the collective's pieces in source order: segment i at i * seg_bytes
+    if w.coll == "allgather":
+        assert np.array_equal(stage.numpy(), s.ref)
+
+
+def test_host_staged_copy_engine_rejects_a_wrong_bounce_buffer(c3):
+    """A bounce buffer in device memory, one too small, or sources that are
+    already page-locked host memory are argument errors, with nothing run."""
+    s = Setup(c3, "tiny_ag")
+    w = s.w
+
+    def run(stage, shards):
+        p = c3.Problem(s.dA, s.dB, s.dC, w.M, w.N, w.K, c3.C3_COLL_ALLGATHER, s.out, w.unit_bytes, w.nranks,
+                       shards=shards, ce_variant=c3.C3_CE_HOST_STAGED, ce_stage=stage)
+        t = c3.C3Timing()
+        return c3.lib().c3_run(ctypes.byref(p.rec), 2, 0, 0, ctypes.byref(t))
+
+    dev_stage = torch.empty(w.coll_bytes, dtype=torch.uint8, device="cuda")
+    assert run(dev_stage, s.dshards) == c3.C3_EINVAL
+    small = torch.empty(w.coll_bytes - 16, dtype=torch.uint8).pin_memory()
+    assert run(small, s.dshards) == c3.C3_EINVAL
+    pageable = torch.empty(w.coll_bytes, dtype=torch.uint8)
+    assert run(pageable, s.dshards) == c3.C3_EINVAL
+    host_shards = [torch.from_numpy(x).pin_memory() for x in I.coll_payload(w)]
+    ok_stage = torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory()
+    assert run(ok_stage, host_shards) == c3.C3_EUNSUP
+
+
+def test_host_staged_copy_engine_cuts_segments_into_pieces(c3):
+    """Shards of 40 MiB + 16 bytes go through the bounce buffer in pieces of
+    16, 16 and 8 MiB + 16 bytes (ragged last piece), byte-exact."""
+    nranks, shard = 8, (40 << 20) + 16
+    payload = [I.random_bytes(3000 + r, shard) for r in range(nranks)]
+    ref = oracle.allgather(payload)
+    dsh = [torch.from_numpy(x).cuda() for x in payload]
+    out = torch.full((nranks * shard,), 0xEE, dtype=torch.uint8, device="cuda")
+    A = torch.zeros((128, 128), dtype=torch.int16, device="cuda")
+    C = torch.empty((128, 128), dtype=torch.float32, device="cuda")
+    stage = torch.empty(nranks * shard, dtype=torch.uint8).pin_memory()
+    p = c3.Problem(A, A, C, 128, 128, 128, c3.C3_COLL_ALLGATHER, out, shard, nranks, shards=dsh,
+                   ce_variant=c3.C3_CE_HOST_STAGED, ce_stage=stage)
+    t = c3.c3_run(p, 2, 0, 0)
+    assert t["status"] == 0
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert float(C.abs().max()) == 0.0

@@ -245,7 +245,7 @@ def test_allreduce_bit_exact(c3, engine, nranks, count):
 
 
 @pytest.mark.parametrize("mode,split,prio", [(1, 0, 0), (1, 0, 1), (1, 16, 0), (2, 0, 0), (2, 8, 0), (0, 0, 0), (3, 0, 0)])
-@pytest.mark.parametrize("variant", [0, 2])
+@pytest.mark.parametrize("variant", [0, 2, 4])
 def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
     w = I.WORKLOADS["tiny_ar"]
     A, B = I.gemm_operands(w)
@@ -255,8 +255,10 @@ def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
     dC = torch.full((w.M, w.N), float("nan"), device="cuda")
     dins = [torch.from_numpy(b).cuda() for b in bufs]
     out = torch.full((w.coll_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    # the host-staged variant bounces the all-gather half through page-locked host memory
+    stage = torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory() if variant == 4 else None
     p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLREDUCE, out, w.unit_bytes, w.nranks, shards=dins,
-                   ce_variant=variant)
+                   ce_variant=variant, ce_stage=stage)
     t = c3.c3_run(p, mode, split, prio)
     assert t["status"] == 0
     _ar_check(out, bufs)
