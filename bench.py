@@ -443,7 +443,12 @@ class ClockSampler:
             self.reader.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        """Median SM clock over the timed region (mostly the idle settle
+        periods between phases, by design), its 10th percentile and minimum
+        (samples that land inside a GEMM phase, which a GB300 runs below its
+        maximum clock under its power limit), the throttle reasons seen and
+        the highest power drawn."""
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -454,13 +459,24 @@ class ClockSampler:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[3]))
+            except ValueError:
+                pass
             for name, flag in zip(names, parts[5:9]):
                 if flag.lower() == "active":
                     reasons.add(name)
         if not sm:
             return None
+        q = sorted(sm)
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_p10": q[len(q) // 10], "sm_mhz_min": q[0],
+                "power_w_max": max(pw) if pw else None,
+                "basis": "nvidia-smi every 200 ms over the timed region (settle periods included)"}
+
+    def samples(self):
+        """The raw sample lines (for the detail output)."""
+        return list(self.lines)
 
 
 # ---------------------------------------------------------------- distributed
@@ -575,9 +591,9 @@ def cpu_c3(w, steps, warmup, rows=None, target_s=1.0):
         t0 = time.perf_counter(); th.start(); gemm(); th.join(); tconc = time.perf_counter() - t0
         if it >= warmup:
             recs.append((tg, tc, tconc))
-    sample = (f"{rows} of {w.M} rows of A against all {w.N}x{w.K} of B (oracle fp64 GEMM, {g_threads} threads) "
-              f"and {unit} B per {dict(allgather='shard', alltoall='block').get(w.coll, 'rank vector')} ({frac:.4f} of the "
-              f"collective, oracle byte loop, 1 thread), isolated then concurrent")
+    sample = (f"{rows}/{w.M} rows of A x all {w.N}x{w.K} of B (fp64 GEMM, {g_threads} threads) + {unit} B per "
+              f"{dict(allgather='shard', alltoall='block').get(w.coll, 'rank vector')} ({frac:.4f} of the collective, "
+              f"byte loop, 1 thread); isolated, then concurrent")
     return recs, sample, cores
 
 
@@ -1035,7 +1051,7 @@ def main(argv=None):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks[key], "unit": "TFLOP/s",
                 "frac": achieved / peaks[key],
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                "peak_source": (f"{peaks['source']} bf16, burst (each phase starts after a {settle_us} us idle period)"
+                "peak_source": (f"{peaks['source']} bf16 burst (phases start after {settle_us} us idle)"
                                 if settle_us > 0 else
                                 f"{peaks['source']} bf16, sustained (phases back to back inside the step)")}
     roof["traffic"] = profiled_traffic(w.name)
@@ -1098,6 +1114,7 @@ def main(argv=None):
         "device": {"name": torch.cuda.get_device_name(dev), **info},
     }
     detail["clocks"] = clk.summary()
+    detail["clock_samples"] = clk.samples()
     if rank == 0:
         emit_detail(detail, args.detail_out)
 
@@ -1177,7 +1194,7 @@ def headline_line(d):
                           if croof else None),
         "gpu_launches": d.get("gpu_launches"),
         "validation": {k: d["validation"][k] for k in ("collective_bit_exact", "gemm_rows_in_tolerance")},
-        "clocks": d.get("clocks"),
+        "clocks": ({k: v for k, v in d["clocks"].items() if k != "basis"} if d.get("clocks") else None),
     }
     for key in ("gemm_bound", "coll_bound"):
         if key in d:
