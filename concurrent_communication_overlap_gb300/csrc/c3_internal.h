@@ -162,8 +162,13 @@ CopyGroup copy_group(DeviceState& ds, int total_ctas, int first_ctas);
 // gate_need > 0: each CTA of this launch first reads st->gemm_started and, if
 // fewer than gate_need GEMM CTAs have started, leaves at once without work (it
 // was dispatched before a GEMM whose CTAs still wait for SMs).
+// dependent: launched with programmatic stream serialization, right after the
+// GEMM on the GEMM's stream, so that the hardware schedules it only once every
+// GEMM CTA has started (the GEMM signals griddepcontrol.launch_dependents on
+// entry); the launch does not wait for the GEMM to finish.
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
-                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need = 0);
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need = 0,
+                   bool dependent = false);
 // Largest number of work units (64 KiB rounds / 32 KiB chunks) a collective may
 // have: the 32-bit counters stay far from wrapping.
 bool copy_units_fit(const SegTable& t);

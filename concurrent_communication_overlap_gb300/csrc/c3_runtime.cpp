@@ -369,18 +369,23 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
 // the GEMM, so its CTAs start only on SMs the GEMM has left: the collective
 // widens to them once the GEMM's CTAs finish (a CTA that finds no work left
 // exits at once).  An all-reduce's copies wait for its reduce-scatter.
+// `dependent`: s2 is the GEMM's stream and this launch directly follows the
+// GEMM there, as its programmatic dependent (not for an all-reduce, whose
+// copies must also wait for the reduce-scatter).
 static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, int l2_stream, int first, int rest,
-                            const CopyGroup& g, cudaStream_t s2, int* ctas, unsigned gemm_ctas) {
+                            const CopyGroup& g, cudaStream_t s2, int* ctas, unsigned gemm_ctas,
+                            bool dependent = false) {
     if (ctas) *ctas = 0;
     const SegTable& t = cp.seg;
     if (rest <= 0 || t.nseg == 0 || t.seg_bytes == 0) return 0;
+    if (dependent && cp.has_rs) return set_error(C3_EINVAL, "an all-reduce's copies cannot follow the GEMM directly");
     if (cp.has_rs) {
         cudaError_t e = cudaStreamWaitEvent(s2, ds.ev[7], 0);
         if (e != cudaSuccess) return set_cuda_error(e, "wait for the reduce-scatter");
     }
     const int flavour = pick_flavour(t, sm_kernel, true);
     const int reserve = flavour == kSmkVec ? exclusive_reserve(ds) : 0;
-    return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas, gemm_ctas);
+    return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas, gemm_ctas, dependent);
 }
 
 // A split group whose second part could not be launched would never count to
@@ -608,18 +613,36 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // claim whatever work is left -- so a collective that outlasts the
         // GEMM widens onto its SMs, and one that finishes first leaves nothing
         // for them but an immediate exit.
+        //
+        // The second part goes out right behind the GEMM on the GEMM's stream,
+        // as its programmatic dependent: the hardware schedules it once every
+        // GEMM CTA has started (each signals griddepcontrol.launch_dependents
+        // on entry), so it can only take SMs the GEMM leaves, and it does not
+        // wait for the GEMM to finish.  The first part, which creates the
+        // launch group, therefore goes out before the GEMM, and the GEMM's
+        // completion event follows the second part: t_gemm_ev then covers
+        // the GEMM's stream (GEMM and the collective's second part).  An
+        // all-reduce's copies must also wait for its reduce-scatter; its
+        // second part keeps a stream of its own and the gemm_started gate.
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
+        const bool dep_rest = part && !t.has_rs;
         const int comm_budget = part ? sm_split : p->comm_sms;
         cudaStream_t sc2 = ds.s_comm_b;
         cudaEvent_t ev_c2 = ds.ev[6];
         CopyGroup grp;
         int cctas2 = 0;
         bool comm_launched = false, rest_launched = false;
-        if (part && (e = cudaStreamWaitEvent(sc2, ev0, 0)) != cudaSuccess) return set_cuda_error(e, "fork");
-        // Each completion event is recorded right after its own launch, before
+        if (part && !dep_rest && (e = cudaStreamWaitEvent(sc2, ev0, 0)) != cudaSuccess)
+            return set_cuda_error(e, "fork");
+        // Each completion event is recorded right after its own launch(es), before
         // anything else is submitted.
         auto go_gemm = [&] {
             int r = gemm_enqueue(gl, sg, ds.status, &gctas);
+            if (r == C3_OK && dep_rest) {
+                r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sg,
+                                     &cctas2, (unsigned)gctas, true);
+                rest_launched = (r == C3_OK);
+            }
             if (r == C3_OK && (e = cudaEventRecord(ev_g, sg)) != cudaSuccess) r = set_cuda_error(e, "event record");
             return r;
         };
@@ -631,7 +654,7 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
             return r;
         };
         auto go_rest = [&] {
-            if (!part) return (int)C3_OK;
+            if (!part || dep_rest) return (int)C3_OK;
             // gated on the GEMM: its CTAs leave at once while GEMM CTAs still wait for SMs
             int r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sc2,
                                      &cctas2, (unsigned)gctas);
@@ -648,10 +671,10 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
                 if (part && !rest_launched) abandon_group(grp, sc);
                 if (cudaEventRecord(ev_c, sc) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c, 0);
             }
-            if (rest_launched && cudaEventRecord(ev_c2, sc2) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c2, 0);
+            if (rest_launched && !dep_rest && cudaEventRecord(ev_c2, sc2) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c2, 0);
             return code;
         };
-        if (priority || reclaim) {
+        if (priority || reclaim || dep_rest) {
             if ((rc = go_comm())) return fail(rc);
             if ((rc = go_gemm())) return fail(rc);
         } else {
@@ -660,8 +683,8 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         }
         if ((rc = go_rest())) return fail(rc);
         if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
-        if (part && (e = cudaStreamWaitEvent(s0, ev_c2, 0)) != cudaSuccess) return set_cuda_error(e, "join");
-        split_rest = part;
+        if (part && !dep_rest && (e = cudaStreamWaitEvent(s0, ev_c2, 0)) != cudaSuccess) return set_cuda_error(e, "join");
+        split_rest = part && !dep_rest;
         cctas += cctas2;
     }
     if ((e = cudaEventRecord(ev_end, s0)) != cudaSuccess) return set_cuda_error(e, "event record");

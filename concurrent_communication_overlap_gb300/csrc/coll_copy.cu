@@ -394,8 +394,27 @@ bool copy_units_fit(const SegTable& t) {
     return copy_units(t, 4 * 1024) < (1ull << 31);
 }
 
+// One launch of `kernel` (a copy kernel instantiation) with the common
+// arguments; `dependent` adds programmatic stream serialization.
+template <class K>
+static cudaError_t launch_copy(K kernel, int ctas, int threads, int smem, cudaStream_t s, bool dependent,
+                               const SegTable& t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
+                               unsigned su, unsigned gate_need) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = dependent ? attr : nullptr;
+    cfg.numAttrs = dependent ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kernel, t, st, work, cta_base, total_ctas, su, gate_need);
+}
+
 int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g, int flavour, int smem_reserve,
-                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need) {
+                   int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need, bool dependent) {
     if (ctas_out) *ctas_out = 0;
     if (t.nseg <= 0 || t.seg_bytes == 0) return 0;
     if (!g.work || g.total_ctas < ctas || cta_base < 0 || cta_base + ctas > g.total_ctas || g.static_ctas < 0 ||
@@ -405,20 +424,17 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) return set_error(-1, "copy launch needs at least one CTA");
     // the group's first part (its first g.static_ctas CTAs) starts on fixed units
+    cudaError_t e;
     if (flavour == kSmkBulk) {
         const unsigned su = (unsigned)g.static_ctas * (unsigned)kBulkBufs;
-        if (l2_stream)
-            copy_bulk_kernel<true><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
-        else
-            copy_bulk_kernel<false><<<ctas, kBulkThreads, kBulkSmem, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
+        e = launch_copy(l2_stream ? copy_bulk_kernel<true> : copy_bulk_kernel<false>, ctas, kBulkThreads, kBulkSmem,
+                        s, dependent, t, st, g.work, cta_base, g.total_ctas, su, gate_need);
     } else {
         const unsigned su = (unsigned)g.static_ctas * (unsigned)kVecWarps;
-        if (l2_stream)
-            copy_vec_kernel<true><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
-        else
-            copy_vec_kernel<false><<<ctas, kVecThreads, smem_reserve, s>>>(t, st, g.work, cta_base, g.total_ctas, su, gate_need);
+        e = launch_copy(l2_stream ? copy_vec_kernel<true> : copy_vec_kernel<false>, ctas, kVecThreads, smem_reserve,
+                        s, dependent, t, st, g.work, cta_base, g.total_ctas, su, gate_need);
     }
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "copy kernel launch");
     count_launch();
     if (ctas_out) *ctas_out = ctas;

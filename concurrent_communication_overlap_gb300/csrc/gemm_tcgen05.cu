@@ -139,6 +139,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lane = threadIdx.x & 31;
     const int total_tiles = num_m * num_n;
 
+    // A kernel launched after this one on its stream with programmatic stream
+    // serialization (the second part of a partitioned collective) may be
+    // scheduled once every CTA of this grid has passed this point: from then
+    // on no GEMM CTA waits for an SM, and the dependent's CTAs take only the
+    // SMs the GEMM leaves.  A no-op for any other successor.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     if (threadIdx.x == 0) {
         stamp_begin(st, true);
         if (st) atomicAdd(&st->gemm_started, 1u);  // read by collective CTAs that wait for the GEMM's SMs

@@ -322,7 +322,9 @@ typedef struct {
     double pct_ideal_ratio;/* s_real / s_ideal                                       (c3_time) */
     double t_gemm_dev;     /* GEMM kernel window by %globaltimer (first CTA start to last CTA end) */
     double t_comm_dev;     /* SM collective kernel window by %globaltimer (0 for CE) */
-    double t_gemm_ev;      /* fork to GEMM completion, CUDA events */
+    double t_gemm_ev;      /* fork to GEMM completion, CUDA events (partitioned SM modes: to the
+                              completion of the GEMM's stream, which also carries the
+                              collective's second part) */
     double t_comm_ev;      /* fork to collective completion, CUDA events */
     int cls;               /* c3_class of (t_gemm_iso, t_comm_iso)                   (c3_time) */
     int mode, sm_split, priority;
@@ -348,9 +350,10 @@ typedef struct {
  *                    CTA fits beside them) and the GEMM on the others.
  *     priority == 1: schedule prioritisation -- the collective is launched
  *                    first, on the library's highest-priority stream; 0: the
- *                    GEMM is launched first and the collective's stream has
- *                    default priority.  (Pages: c3_sp, c3_rp and their
- *                    combination.)
+ *                    collective's stream has default priority and the GEMM is
+ *                    launched first (with sm_split > 0 the collective's first
+ *                    part still goes first, see below).  (Pages: c3_sp, c3_rp
+ *                    and their combination.)
  *   In every concurrent mode the GEMM runs on p->stream and the collective on
  *   a library stream forked from it by an event and joined back by another.
  *   mode C3_MODE_CONCURRENT_CE: the collective as driver memcpy transfers on
@@ -366,15 +369,21 @@ typedef struct {
  *     The partition lasts as long as the collective, not as long as the GEMM.
  *     priority has no further effect in this mode.
  *   In both partitioned modes the collective is one launch group of SM-count
- *   CTAs: its first sm_split CTAs as above, and the rest launched after the
- *   GEMM on another library stream, gated on the GEMM (a CTA that starts while
- *   GEMM CTAs still wait for SMs leaves at once), so they run only on SMs the
- *   GEMM has left: a collective that outlasts the GEMM widens onto them.
+ *   CTAs: its first sm_split CTAs, launched before the GEMM, and the rest,
+ *   launched right behind the GEMM on the GEMM's stream as its programmatic
+ *   dependent (cudaLaunchAttributeProgrammaticStreamSerialization): every GEMM
+ *   CTA signals on entry, so the hardware schedules the rest only once no GEMM
+ *   CTA waits for an SM, and they run only on SMs the GEMM has left -- a
+ *   collective that outlasts the GEMM widens onto them.  t_gemm_ev then times
+ *   the GEMM's stream, the GEMM and that second part.  (All-reduce: its copies
+ *   must also wait for the reduce-scatter, so the rest goes on another library
+ *   stream and is gated instead: a CTA that starts while GEMM CTAs have not all
+ *   started leaves at once, and the collective may then not widen.)
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error
  * (nothing launched) or the device status of the run.  If a launch fails after
- * the collective went out (prioritised and reclaim modes launch it first), the
+ * the collective went out (prioritised and partitioned modes launch it first), the
  * call returns C3_ECUDA with p->stream still ordered after the collective, so
  * the caller may reuse the buffers once that stream has drained.
  */
