@@ -780,7 +780,7 @@ def run_heuristics(args, c3, torch, np, I, dev, info):
     scen = [(w.name, w) for coll in ("allgather", "alltoall")
             for w in I.sweep_workloads(coll, hi_bytes=args.sweep_max_mib << 20)]
     scen.append(("mem_ag", I.WORKLOADS["mem_ag"]))
-    rows, hits = [], 0
+    rows, hits, hits_elastic = [], 0, 0
     cache = {}
     for name, w in scen:
         key = (w.M, w.N, w.K)
@@ -809,12 +809,20 @@ def run_heuristics(args, c3, torch, np, I, dev, info):
         loss = meas[pk] / meas[best_k] - 1.0
         hit = pk == best_k or loss <= 0.015
         hits += hit
+        # the same table with this library's elastic partitions modelled (c3_rp_predict_elastic)
+        ek, _, _ = c3.c3_rp_predict(table, w.gemm_flops, w.gemm_bytes, w.coll_bytes, peaks["bf16_tflops"] * 1e12,
+                                    peaks["hbm_gbs"] * 1e9, elastic=True)
+        eloss = meas[ek] / meas[best_k] - 1.0
+        ehit = ek == best_k or eloss <= 0.015
+        hits_elastic += ehit
         rows.append({"scenario": name, "best_sms": best_k, "predicted_sms": pk, "loss_pct": 100 * loss, "hit": hit,
+                     "predicted_sms_elastic": ek, "loss_pct_elastic": 100 * eloss, "hit_elastic": ehit,
                      "t_conc_us": {str(k): 1e6 * v for k, v in meas.items()}})
         del sh, send, o, p
     print(json.dumps({"heuristics": "rp", "table": [{"sms": k, "gemm_compute": gc, "gemm_memory": gm, "coll": co}
                                                     for k, gc, gm, co in table],
-                      "scenarios": len(rows), "hits": hits, "rows": rows, "peaks": peaks}), flush=True)
+                      "scenarios": len(rows), "hits": hits, "hits_elastic": hits_elastic, "rows": rows,
+                      "peaks": peaks}), flush=True)
     return 0
 
 

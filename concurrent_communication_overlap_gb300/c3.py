@@ -112,6 +112,9 @@ def _load():
         "c3_rp_predict": [ctypes.POINTER(C3RpTable), ctypes.c_double, ctypes.c_double, ctypes.c_double,
                           ctypes.c_double, ctypes.c_double, ctypes.POINTER(_int), ctypes.POINTER(ctypes.c_double),
                           ctypes.POINTER(ctypes.c_double)],
+        "c3_rp_predict_elastic": [ctypes.POINTER(C3RpTable), ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                  ctypes.c_double, ctypes.c_double, ctypes.POINTER(_int),
+                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
         "c3_gemm_plan": [_i64, _i64, _i64, _int, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)],
         "c3_cta_windows": [_int, ctypes.POINTER(C3CtaWindow), _int, ctypes.POINTER(_int)],
     }
@@ -130,7 +133,7 @@ _lib = _load()
 EXPORTED = ("c3_get_device_info", "c3_strerror", "c3_last_error", "c3_status_check", "c3_shutdown",
             "c3_gemm", "c3_allgather", "c3_alltoall", "c3_allreduce", "c3_run", "c3_time", "c3_l2_flush", "c3_kernel_launches",
             "c3_gemm_noalloc", "c3_gemm_plan", "c3_selftest_wait", "c3_inject_fault", "c3_sp_predict",
-            "c3_rp_predict", "c3_cta_windows")
+            "c3_rp_predict", "c3_rp_predict_elastic", "c3_cta_windows")
 
 
 def lib():
@@ -247,18 +250,20 @@ def c3_sp_predict(gemm_ctas, coll_ctas):
     return rc
 
 
-def c3_rp_predict(table, gemm_flops, gemm_bytes, coll_bytes, peak_flops, peak_bytes_per_s):
+def c3_rp_predict(table, gemm_flops, gemm_bytes, coll_bytes, peak_flops, peak_bytes_per_s, elastic=False):
     """table: list of (sms, gemm_compute_slowdown, gemm_memory_slowdown, coll_slowdown).
-    Returns (best_sms, predicted_seconds, [prediction per entry])."""
+    Returns (best_sms, predicted_seconds, [prediction per entry]).  elastic: the
+    model of partitions that dissolve when the GEMM ends (c3_rp_predict_elastic)."""
+    fn = _lib.c3_rp_predict_elastic if elastic else _lib.c3_rp_predict
     t = C3RpTable()
     t.n = len(table)
     for i, (k, gc, gm, co) in enumerate(table):
         t.sms[i], t.gemm_compute[i], t.gemm_memory[i], t.coll[i] = int(k), float(gc), float(gm), float(co)
     best, tp = _int(), ctypes.c_double()
     each = (ctypes.c_double * C3_RP_MAX)()
-    _check(_lib.c3_rp_predict(ctypes.byref(t), float(gemm_flops), float(gemm_bytes), float(coll_bytes),
-                              float(peak_flops), float(peak_bytes_per_s), ctypes.byref(best), ctypes.byref(tp),
-                              each), "c3_rp_predict")
+    _check(fn(ctypes.byref(t), float(gemm_flops), float(gemm_bytes), float(coll_bytes), float(peak_flops),
+              float(peak_bytes_per_s), ctypes.byref(best), ctypes.byref(tp), each),
+           "c3_rp_predict_elastic" if elastic else "c3_rp_predict")
     return best.value, tp.value, [each[i] for i in range(t.n)]
 
 

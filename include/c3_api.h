@@ -492,6 +492,16 @@ int c3_inject_fault(int site);
  * Returns its SM count in *best_sms and its predicted time (s) in
  * *t_pred_best; t_pred_each (may be NULL) receives all n predictions.  Host
  * only; C3_EINVAL on empty tables, non-positive entries or sizes.
+ *
+ * c3_rp_predict_elastic: the same, for this library's partitions, which
+ * dissolve when the GEMM ends (c3_run: the collective's second part widens
+ * onto the SMs the GEMM leaves).  Where the collective would outlast the
+ * GEMM (T_comm * coll[i] > T_gemm * slowdown_gemm[i]), it has moved the share
+ * T_gemm * slowdown_gemm[i] / (T_comm * coll[i]) of its bytes by the time the
+ * GEMM ends and moves the rest at the every-SM rate, so the prediction is
+ *     T_comm + T_gemm * slowdown_gemm[i] * (1 - 1 / coll[i]);
+ * otherwise it is the GEMM's scaled time, as in c3_rp_predict.  Same
+ * arguments, outputs and errors.
  */
 #define C3_RP_MAX 16
 typedef struct {
@@ -506,6 +516,9 @@ int c3_sp_predict(int gemm_ctas, int coll_ctas);
 int c3_rp_predict(const c3_rp_table *t, double gemm_flops, double gemm_bytes, double coll_bytes,
                   double peak_flops, double peak_bytes_per_s, int *best_sms, double *t_pred_best,
                   double *t_pred_each);
+int c3_rp_predict_elastic(const c3_rp_table *t, double gemm_flops, double gemm_bytes, double coll_bytes,
+                          double peak_flops, double peak_bytes_per_s, int *best_sms, double *t_pred_best,
+                          double *t_pred_each);
 
 /*
  * Per-CTA windows of the last run (diagnostics; the pages have no

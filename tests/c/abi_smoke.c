@@ -31,6 +31,7 @@ static const any_fn k_entry_points[] = {
     (any_fn)c3_allgather,       (any_fn)c3_alltoall,     (any_fn)c3_allreduce,     (any_fn)c3_run,
     (any_fn)c3_time,            (any_fn)c3_gemm_noalloc, (any_fn)c3_selftest_wait, (any_fn)c3_inject_fault,
     (any_fn)c3_sp_predict,      (any_fn)c3_rp_predict,   (any_fn)c3_l2_flush,      (any_fn)c3_cta_windows,
+    (any_fn)c3_rp_predict_elastic,
 };
 
 #define N_RANKS 8

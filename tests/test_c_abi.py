@@ -37,7 +37,7 @@ def test_header_compiles_as_c99_and_links_every_entry_point(tmp_path):
     exe = _build(tmp_path)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert "20 entry points" in r.stdout
+    assert "21 entry points" in r.stdout
 
 
 @pytest.mark.gpu
