@@ -591,9 +591,8 @@ def cpu_c3(w, steps, warmup, rows=None, target_s=1.0):
         t0 = time.perf_counter(); th.start(); gemm(); th.join(); tconc = time.perf_counter() - t0
         if it >= warmup:
             recs.append((tg, tc, tconc))
-    sample = (f"{rows}/{w.M} rows of A x all {w.N}x{w.K} of B (fp64 GEMM, {g_threads} threads) + {unit} B per "
-              f"{dict(allgather='shard', alltoall='block').get(w.coll, 'rank vector')} ({frac:.4f} of the collective, "
-              f"byte loop, 1 thread); isolated, then concurrent")
+    sample = (f"{rows}/{w.M} rows of A x all of B (fp64, {g_threads} threads); {frac:.4f} of the collective "
+              f"(1 thread); isolated, then concurrent")
     return recs, sample, cores
 
 
@@ -1214,7 +1213,7 @@ def headline_line(d):
                                                 "engine", "mode")}
     line = _sig(line)
     # stay under the cap whatever the strings hold: drop the least needed keys first
-    for key in ("modes_pct", "roofline_copy", "clocks"):
+    for key in ("roofline_copy", "modes_pct", "clocks"):
         if len(json.dumps(line)) <= HEADLINE_MAX_BYTES:
             break
         line.pop(key, None)

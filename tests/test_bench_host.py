@@ -188,6 +188,30 @@ def test_headline_line_keeps_every_mode_share_when_it_fits():
     assert line["value"] == pytest.approx(19.877, rel=1e-4)       # 5 significant digits
 
 
+def test_headline_of_the_default_run_keeps_every_mode_share():
+    """The default run's own shape: the 405B-shaped pair's nine modes, the full
+    clock record, the real peak-source and CPU-sample wordings; every mode's
+    share stays in the line, under the cap."""
+    import json
+    d = _synthetic_detail(0)
+    names = [m[0] for m in bench.select_modes("l405_a2a")]
+    d["modes"] = {n: {"pct_ideal_gain": -123.456789 + i} for i, n in enumerate(names)}
+    d["config"] = {"workload": "l405_a2a", "M": 8192, "N": 53248, "K": 16384,
+                   "collective": "alltoall 8 ranks x 8388608 B", "coll_src": "device",
+                   "l2": "flushed before every timed phase (2 x L2 zero-fill)", "parallelism": "single GPU"}
+    d["settle_us"] = 18828
+    d["roofline"]["peak_source"] = "measured bf16 burst (phases start after 18828 us idle)"
+    d["clocks"] = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 315, "sm_mhz_p10": 2070.0,
+                   "sm_mhz_min": 2070.0, "power_w_max": 556.97,
+                   "basis": "nvidia-smi every 200 ms over the timed region (settle periods included)"}
+    d["cpu_baseline"]["sample"] = ("8/8192 rows of A x all of B (fp64, 15 threads); 0.0010 of the collective "
+                                   "(1 thread); isolated, then concurrent")
+    line = bench.headline_line(d)
+    assert set(line["modes_pct"]) == set(names) and len(names) == 9
+    assert "basis" not in line["clocks"] and line["clocks"]["power_w_max"] == pytest.approx(556.97)
+    assert len(json.dumps(line)) <= bench.HEADLINE_MAX_BYTES
+
+
 def test_default_modes_of_the_405b_pair_and_explicit_subsets():
     names = [m[0] for m in bench.select_modes("l405_a2a")]
     for n in ("baseline", "prioritised", "partitioned_8", "partitioned_16", "partitioned_32", "ce", "ce_rp_8",
