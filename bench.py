@@ -1016,6 +1016,10 @@ def main(argv=None):
             "s_ideal": m["s_ideal"], "s_real": m["s_real"],
             "pct_ideal_gain": m["pct_ideal_gain"],
             "pct_ideal_gain_ci95": share_ci95(recs, tc_strict, tg_steps=tg_steps),
+            # the same share from medians (a mode whose runs come in slow bursts, as the
+            # copy through host memory does on a busy link, reads very differently)
+            "pct_ideal_gain_from_medians": pct_gain(statistics.median(tg_steps), tc_strict,
+                                                    statistics.median([r["t_conc"] for r in recs]))["pct_ideal_gain"],
             "t_gemm_iso_own_us": 1e6 * step_mean([r["t_gemm_iso"] for r in recs]),
             "pct_ideal_ratio": m["pct_ideal_ratio"],
             "pct_ideal_gain_own_engine": m_own["pct_ideal_gain"], "s_ideal_own_engine": m_own["s_ideal"],
