@@ -18,6 +18,10 @@ struct CtaRec {
 
 constexpr int kCtaRecs = 256;      // CTAs recorded per kernel (the first 256)
 constexpr int kSchedSlots = 64;    // GEMM tile-scheduler counters, used round-robin by launches
+constexpr int kMaxRanksAr = 8;     // ranks of an all-reduce
+// Words of one SM-collective work slot: the next unit, the CTAs done, and per
+// all-reduce chunk the reduce-scatter pieces finished.
+constexpr int kCollSlotWords = 2 + kMaxRanksAr;
 
 // Device status block (library-owned, reset before each timed run).
 struct DevStatus {
@@ -39,12 +43,12 @@ struct DevStatus {
     // the per-run reset leaves them alone (a GEMM of another stream may be
     // using a slot).
     unsigned int sched[kSchedSlots][2];
-    // Work counters of the SM copy kernels, the same way: per slot, the next
-    // work unit (a 64 KiB round or a 32 KiB chunk) and the number of CTAs
-    // done.  One slot serves a launch group -- one launch, or several on
-    // different streams that share the collective's work -- and its last CTA
-    // puts the slot back to zero.
-    unsigned int coll_sched[kSchedSlots][2];
+    // Work counters of the SM collective kernels, the same way: per slot, the
+    // next work unit and the number of CTAs done, then (all-reduce) per chunk
+    // the reduce-scatter pieces finished.  One slot serves a launch group --
+    // one launch, or several on different streams that share the collective's
+    // work -- and its last CTA puts the slot back to zero.
+    unsigned int coll_sched[kSchedSlots][kCollSlotWords];
 };
 
 constexpr size_t kStatusBytes = 16384;
@@ -54,8 +58,6 @@ constexpr int kMaxSegs = 64;
 
 // A collective as a list of equal-size byte segments src[i] -> dst[i].
 enum { kSegAllGather = 0, kSegAllToAll = 1, kSegAllReduce = 2 };
-
-constexpr int kMaxRanksAr = 8;
 
 // The reduce-scatter half of an all-reduce of nranks fp32 vectors of `count`
 // elements: chunk c (count / nranks elements) of the rank-order sum goes to
@@ -175,6 +177,13 @@ bool copy_units_fit(const SegTable& t);
 int copy_init_device(int max_reserve);
 int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStream_t s, DevStatus* st,
                           int* ctas_out);
+// The whole all-reduce on SMs (reduce-scatter `r` and the all-gather `t` of
+// its chunks) as one launch of a launch group, the group's counters as for
+// copy_sm_launch: `ctas` CTAs numbered from cta_base; gate_need and dependent
+// as for copy_sm_launch.
+int allreduce_sm_launch(const RsTable& r, const SegTable& t, int ctas, int cta_base, const CopyGroup& g,
+                        int smem_reserve, int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out,
+                        unsigned gate_need = 0, bool dependent = false);
 int bulk_copy_smem_bytes();
 
 // `stage`: the page-locked host bounce buffer of kCeHostStaged (at least

@@ -323,6 +323,17 @@ static int pick_flavour(const SegTable& t, int sm_kernel, bool exclusive) {
            : (exclusive && !t.host_src ? kSmkBulk : kSmkVec);
 }
 
+// A partitioned all-reduce on the SM engine (a launch group split in two
+// parts) runs on the fused all-reduce kernel: sums and copies claimed from
+// one counter, so the whole all-reduce widens onto the SMs a GEMM leaves.
+// Every other all-reduce -- unsplit, on the copy engine, or with the bulk
+// copy kernel asked for -- runs as the reduce-scatter kernel followed by the
+// copies (two launches, each over its whole grid at once: the faster form
+// when nothing has to widen).
+static bool ar_fused(const CollPlan& cp, int engine, int sm_kernel, bool split) {
+    return cp.has_rs && engine == C3_ENGINE_SM && sm_kernel != C3_SMK_BULK && split;
+}
+
 // One collective launch.  SM engine: `budget` CTAs (0 = default), one launch
 // group; exclusive = the CTAs keep their SMs to themselves (partitioning).
 // With `split_total` > budget the collective is the first part of a split
@@ -339,6 +350,13 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
     const int total = split_total > k ? split_total : k;
     if (engine == C3_ENGINE_SM && t.host_src && sm_kernel == C3_SMK_BULK)
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only; host sources take the vector kernel");
+    if (ar_fused(cp, engine, sm_kernel, split_total > k)) {
+        // the whole all-reduce in one launch group (its rest from launch_coll_rest)
+        CopyGroup g = copy_group(ds, total, k);
+        if (group) *group = g;
+        return allreduce_sm_launch(cp.rs, t, k, 0, g, exclusive ? exclusive_reserve(ds) : 0, l2_stream, s, ds.status,
+                                   ctas);
+    }
     if (cp.has_rs) {
         // the reduce-scatter needs arithmetic: always SMs, whatever the engine
         int rc = reduce_scatter_launch(cp.rs, k, exclusive ? exclusive_reserve(ds) : 0, s, ds.status, ctas);
@@ -368,17 +386,24 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
 // from `first`, exclusive like the first part, on stream `s2`.  Launched after
 // the GEMM, so its CTAs start only on SMs the GEMM has left: the collective
 // widens to them once the GEMM's CTAs finish (a CTA that finds no work left
-// exits at once).  An all-reduce's copies wait for its reduce-scatter.
+// exits at once).  An all-reduce on the fused kernel launches the rest of
+// that kernel's group; one run as the reduce-scatter kernel and copies has
+// its copies wait for the reduce-scatter launch.
 // `dependent`: s2 is the GEMM's stream and this launch directly follows the
-// GEMM there, as its programmatic dependent (not for an all-reduce, whose
-// copies must also wait for the reduce-scatter).
+// GEMM there, as its programmatic dependent (not for the reduce-scatter
+// kernel's copies, which must also wait for that launch).
 static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, int l2_stream, int first, int rest,
                             const CopyGroup& g, cudaStream_t s2, int* ctas, unsigned gemm_ctas,
                             bool dependent = false) {
     if (ctas) *ctas = 0;
     const SegTable& t = cp.seg;
-    if (rest <= 0 || t.nseg == 0 || t.seg_bytes == 0) return 0;
-    if (dependent && cp.has_rs) return set_error(C3_EINVAL, "an all-reduce's copies cannot follow the GEMM directly");
+    if (rest <= 0) return 0;
+    if (ar_fused(cp, C3_ENGINE_SM, sm_kernel, true))
+        return allreduce_sm_launch(cp.rs, t, rest, first, g, exclusive_reserve(ds), l2_stream, s2, ds.status, ctas,
+                                   gemm_ctas, dependent);
+    if (t.nseg == 0 || t.seg_bytes == 0) return 0;
+    if (dependent && cp.has_rs)
+        return set_error(C3_EINVAL, "an all-reduce's copies after the reduce-scatter kernel cannot follow the GEMM directly");
     if (cp.has_rs) {
         cudaError_t e = cudaStreamWaitEvent(s2, ds.ev[7], 0);
         if (e != cudaSuccess) return set_cuda_error(e, "wait for the reduce-scatter");
@@ -392,7 +417,7 @@ static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, 
 // its total, so its work counter would stay dirty: clear it behind the first
 // part, on the first part's stream.
 static void abandon_group(const CopyGroup& g, cudaStream_t s) {
-    if (g.work) cudaMemsetAsync(g.work, 0, 2 * sizeof(unsigned int), s);
+    if (g.work) cudaMemsetAsync(g.work, 0, kCollSlotWords * sizeof(unsigned int), s);
 }
 
 static int wait_event(cudaEvent_t ev, double limit_s) {
@@ -622,10 +647,13 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // launch group, therefore goes out before the GEMM, and the GEMM's
         // completion event follows the second part: t_gemm_ev then covers
         // the GEMM's stream (GEMM and the collective's second part).  An
-        // all-reduce's copies must also wait for its reduce-scatter; its
-        // second part keeps a stream of its own and the gemm_started gate.
+        // all-reduce on the fused kernel is such a group too (its copies wait
+        // for their chunk's sums inside the kernel).  One run as the
+        // reduce-scatter kernel and bulk copies must have its copies wait for
+        // the reduce-scatter launch: its second part keeps a stream of its own
+        // and the gemm_started gate.
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
-        const bool dep_rest = part && !t.has_rs;
+        const bool dep_rest = part && (!t.has_rs || ar_fused(t, engine, p->sm_kernel, true));
         const int comm_budget = part ? sm_split : p->comm_sms;
         cudaStream_t sc2 = ds.s_comm_b;
         cudaEvent_t ev_c2 = ds.ev[6];

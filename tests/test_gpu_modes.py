@@ -150,6 +150,91 @@ def test_partitioned_collective_widens_onto_the_sms_the_gemm_leaves(c3, mode, pr
     assert t["comm_sms"] > 64, t
 
 
+@pytest.mark.parametrize("mode,prio", [(1, 0), (1, 1), (4, 0)])
+def test_partitioned_allreduce_widens_onto_the_sms_the_gemm_leaves(c3, mode, prio):
+    """The same one-tile GEMM beside an all-reduce of eight 8 M-element fp32
+    vectors partitioned onto 8 SMs: the fused all-reduce kernel is one launch
+    group, so its second part takes the SMs the GEMM leaves for both halves
+    (the sums and the copies of each chunk); the output is the oracle's
+    rank-order sum bit for bit and no SM holds both kernels at once."""
+    info = c3.c3_get_device_info()
+    M, N, K = 128, 128, 64
+    A = I.bf16_uniform(23, (M, K))
+    B = I.bf16_uniform(24, (N, K))
+    C_ref, S_ref = oracle.gemm(A, B)
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    R, count = 8, 8 << 20
+    bufs = [I.normal(1100 + r, count).astype(np.float32) for r in range(R)]
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    out = torch.full((R * count,), float("nan"), dtype=torch.float32, device="cuda")
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLREDUCE, out, count * 4, R, shards=dins)
+    t = c3.c3_run(p, mode, 8, prio)
+    assert t["status"] == 0
+    ref, _ = oracle.allreduce(bufs)
+    assert np.array_equal(out.cpu().numpy().reshape(ref.shape).view(np.uint32), ref.view(np.uint32))
+    assert (np.abs(dC.cpu().numpy().astype(np.float64) - C_ref) <= TOL * S_ref).all()
+    assert t["smid_overlap"] == 0, t
+    assert t["comm_ctas"] == info["sm_count"]
+    # 8 SMs alone would need ~1 ms for its ~0.8 GB of traffic; the idle SMs join at once
+    assert t["comm_sms"] > 64, t
+
+
+def _tiny_gemm(seed):
+    M, N, K = 128, 128, 64
+    A = I.bf16_uniform(seed, (M, K))
+    B = I.bf16_uniform(seed + 1, (N, K))
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    return (M, N, K), (A, B), (dA, dB, dC)
+
+
+def test_partitioned_allreduce_work_counters_recycle_over_many_launches(c3):
+    """More partitioned all-reduce runs than work slots (64), with first parts
+    of 1..7 SMs (most sum slices claimed) and of 12..32 SMs (every slice a
+    fixed unit, the copies in fixed rounds), and a poisoned output each time:
+    a claim counter left non-zero would skip units, and a chunk count left
+    non-zero would let the copies run ahead of the sums (copying the poison)."""
+    (M, N, K), _, (dA, dB, dC) = _tiny_gemm(31)
+    R, count = 8, 8 * 3000 + 32          # 3004 elements a chunk: ragged slices and pieces
+    bufs = [I.normal(1200 + r, count).astype(np.float32) for r in range(R)]
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    ref, _ = oracle.allreduce(bufs)
+    ref_t = torch.from_numpy(ref.reshape(-1).copy()).cuda()
+    out = torch.empty(R * count, dtype=torch.float32, device="cuda")
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLREDUCE, out, count * 4, R, shards=dins)
+    splits = [1, 2, 3, 4, 5, 6, 7, 12, 16, 32]
+    for i in range(150):
+        out.fill_(float("nan"))
+        t = c3.c3_run(p, 4 if i % 5 == 4 else 1, splits[i % len(splits)], i % 2)
+        assert t["status"] == 0
+        assert torch.equal(out.view(torch.int32), ref_t.view(torch.int32)), i
+    c3.c3_status_check()
+
+
+@pytest.mark.parametrize("nranks,count", [(8, 1 << 16), (8, 32 * 37), (5, 20 * 9), (2, 8), (1, 4), (1, 4096 + 4)])
+@pytest.mark.parametrize("split", [8, 64])
+def test_partitioned_allreduce_bit_exact(c3, nranks, count, split):
+    """The fused all-reduce kernel (partitioned runs) at rank counts 1..8 and
+    ragged chunks, against the oracle's rank-order fp32 sum."""
+    (M, N, K), (A, B), (dA, dB, dC) = _tiny_gemm(41)
+    bufs = [I.normal(1300 + r, count).astype(np.float32) for r in range(nranks)]
+    bufs[0][:3] = [-0.0, np.inf, 1e38]
+    if nranks > 1:
+        bufs[1][2] = 1e38
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    out = torch.full((nranks * count,), float("nan"), dtype=torch.float32, device="cuda")
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLREDUCE, out, count * 4, nranks, shards=dins)
+    t = c3.c3_run(p, 1, split, 0)
+    assert t["status"] == 0
+    ref, _ = oracle.allreduce(bufs)
+    assert np.array_equal(out.cpu().numpy().reshape(ref.shape).view(np.uint32), ref.view(np.uint32))
+    C_ref, S_ref = oracle.gemm(A, B)
+    assert (np.abs(dC.cpu().numpy().astype(np.float64) - C_ref) <= TOL * S_ref).all()
+
+
 def test_copy_work_counters_recycle_over_many_launches(c3):
     """More collective launches than work-counter slots (64), with launch
     groups of 1..7 CTAs: a counter left non-zero would make a later launch

@@ -244,9 +244,15 @@ def test_allreduce_bit_exact(c3, engine, nranks, count):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("mode,split,prio", [(1, 0, 0), (1, 0, 1), (1, 16, 0), (2, 0, 0), (2, 8, 0), (0, 0, 0), (3, 0, 0)])
+@pytest.mark.parametrize("mode,split,prio,flavour", [
+    (1, 0, 0, 0), (1, 0, 1, 0), (1, 16, 0, 0), (1, 16, 1, 0), (4, 16, 0, 0), (2, 0, 0, 0), (2, 8, 0, 0),
+    (0, 0, 0, 0), (3, 0, 0, 0),
+    # the bulk copy kernel: reduce-scatter kernel, then the copies (gated second part)
+    (1, 0, 0, 2), (1, 16, 0, 2), (4, 16, 0, 2)])
 @pytest.mark.parametrize("variant", [0, 2, 4])
-def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
+def test_allreduce_in_every_mode(c3, mode, split, prio, flavour, variant):
+    if flavour and mode in (2, 3):
+        pytest.skip("the SM copy flavour does not apply to the copy-engine modes")
     w = I.WORKLOADS["tiny_ar"]
     A, B = I.gemm_operands(w)
     bufs = I.coll_payload(w)
@@ -258,7 +264,7 @@ def test_allreduce_in_every_mode(c3, mode, split, prio, variant):
     # the host-staged variant bounces the all-gather half through page-locked host memory
     stage = torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory() if variant == 4 else None
     p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLREDUCE, out, w.unit_bytes, w.nranks, shards=dins,
-                   ce_variant=variant, ce_stage=stage)
+                   ce_variant=variant, ce_stage=stage, sm_kernel=flavour)
     t = c3.c3_run(p, mode, split, prio)
     assert t["status"] == 0
     _ar_check(out, bufs)
