@@ -253,6 +253,9 @@ int c3_alltoall(const void *in, void *out, size_t block_bytes, int nranks, int e
  * Every row ends as out[r][i] = ((0 + in_0[i]) + in_1[i]) + ... + in_{R-1}[i]
  * in fp32, rank order -- the same on every row and bit-reproducible.  The
  * reduce-scatter uses sm_budget SMs (0 = default).  Asynchronous on `s`.
+ * (A partitioned c3_run runs the all-reduce as one fused kernel; see c3_run.
+ * A wait inside that kernel that gives up -- a copy waiting past the 2 s
+ * limit for its chunk's sums -- is C3_ETIMEOUT, as for every bounded wait.)
  */
 int c3_allreduce(const float *const *inputs, float *out, size_t count, int nranks, int engine,
                  int sm_budget, c3_stream s);
@@ -375,10 +378,17 @@ typedef struct {
  *   CTA signals on entry, so the hardware schedules the rest only once no GEMM
  *   CTA waits for an SM, and they run only on SMs the GEMM has left -- a
  *   collective that outlasts the GEMM widens onto them.  t_gemm_ev then times
- *   the GEMM's stream, the GEMM and that second part.  (All-reduce: its copies
- *   must also wait for the reduce-scatter, so the rest goes on another library
- *   stream and is gated instead: a CTA that starts while GEMM CTAs have not all
- *   started leaves at once, and the collective may then not widen.)
+ *   the GEMM's stream, the GEMM and that second part.  An all-reduce on the
+ *   SM engine is such a group too: in both partitioned modes it runs as one
+ *   fused kernel whose warps claim the reduce-scatter's sums and then the
+ *   all-gather's copies from one counter, a copy of a chunk waiting in the
+ *   kernel until that chunk's sums are all written, so the whole all-reduce
+ *   widens.  With p->sm_kernel == C3_SMK_BULK it keeps the reduce-scatter
+ *   kernel and bulk copies: the copies must wait for the reduce-scatter
+ *   launch, so their rest goes on another library stream and is gated instead
+ *   (a CTA that starts while GEMM CTAs have not all started leaves at once,
+ *   and the collective may then not widen).  The result is bit-identical
+ *   either way.
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error
