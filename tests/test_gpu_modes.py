@@ -216,9 +216,11 @@ def test_partitioned_allreduce_work_counters_recycle_over_many_launches(c3):
 
 @pytest.mark.parametrize("nranks,count", [(8, 1 << 16), (8, 32 * 37), (5, 20 * 9), (2, 8), (1, 4), (1, 4096 + 4)])
 @pytest.mark.parametrize("split", [8, 64])
-def test_partitioned_allreduce_bit_exact(c3, nranks, count, split):
+@pytest.mark.parametrize("l2", [0, 1])   # normal, evict-first loads and stores
+def test_partitioned_allreduce_bit_exact(c3, nranks, count, split, l2):
     """The fused all-reduce kernel (partitioned runs) at rank counts 1..8 and
-    ragged chunks, against the oracle's rank-order fp32 sum."""
+    ragged chunks, with either L2 policy, against the oracle's rank-order fp32
+    sum."""
     (M, N, K), (A, B), (dA, dB, dC) = _tiny_gemm(41)
     bufs = [I.normal(1300 + r, count).astype(np.float32) for r in range(nranks)]
     bufs[0][:3] = [-0.0, np.inf, 1e38]
@@ -226,7 +228,7 @@ def test_partitioned_allreduce_bit_exact(c3, nranks, count, split):
         bufs[1][2] = 1e38
     dins = [torch.from_numpy(b).cuda() for b in bufs]
     out = torch.full((nranks * count,), float("nan"), dtype=torch.float32, device="cuda")
-    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLREDUCE, out, count * 4, nranks, shards=dins)
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLREDUCE, out, count * 4, nranks, shards=dins, coll_l2=l2)
     t = c3.c3_run(p, 1, split, 0)
     assert t["status"] == 0
     ref, _ = oracle.allreduce(bufs)
