@@ -337,9 +337,10 @@ static bool ar_fused(const CollPlan& cp, int engine, int sm_kernel, bool split) 
 // One collective launch.  SM engine: `budget` CTAs (0 = default), one launch
 // group; exclusive = the CTAs keep their SMs to themselves (partitioning).
 // With `split_total` > budget the collective is the first part of a split
-// group of split_total CTAs (launch_coll_rest launches the others); the
-// reduce-scatter of an all-reduce then records ds.ev[7], which the rest waits
-// for.  *group receives the group (SM engine).
+// group of split_total CTAs (launch_coll_rest launches the others): an
+// all-reduce then runs on the fused kernel, or, with the bulk copy kernel,
+// its reduce-scatter records ds.ev[7], which the rest waits for.  *group
+// receives the group (SM engine).
 static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_kernel, int l2_stream, int ce_variant,
                        int budget, bool exclusive, cudaStream_t s, int* ctas, int split_total = 0,
                        CopyGroup* group = nullptr) {
