@@ -1128,6 +1128,14 @@ def main(argv=None):
     detail["clock_samples"] = clk.samples()
     if rank == 0:
         emit_detail(detail, args.detail_out)
+        if args.detail_out:
+            # every timed step's phase times (us), in the detail file only: the summaries above
+            # are computed from these
+            steps_rec = {"detail": "steps", "modes": {
+                name: {k: [round(1e6 * r[k], 2) for r in recs] for k in ("t_gemm_iso", "t_comm_iso", "t_conc")}
+                for name, recs in per_mode.items()}}
+            with open(args.detail_out, "a") as fh:
+                fh.write(json.dumps(steps_rec) + "\n")
 
     if not args.no_aux:
         detail["aux"] = aux_measure(c3, torch, w, dev, stream, peaks, dshards, dsend, out, info)
