@@ -300,6 +300,30 @@ def test_gemm_full_size_compute_bound_rows_and_columns(c3, wname):
     assert_gemm_close(got, c_ref, s_ref)
 
 
+@pytest.mark.parametrize("mode,split", [(1, 32), (4, 16)])
+def test_allreduce_full_size_partitioned(c3, mode, split):
+    """The memory-bound all-reduce pair at full size in a partitioned and a
+    reclaim run (the fused all-reduce kernel beside the HBM-bound GEMM): the
+    all-reduce bit-exact against the oracle, sampled GEMM rows within the
+    tolerance."""
+    w = I.WORKLOADS["mem_ar"]
+    A, B = I.gemm_operands(w)
+    bufs = I.coll_payload(w)
+    dA, dB = dev_u16(A), dev_u16(B)
+    dC = torch.full((w.M, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    dins = [torch.from_numpy(b).cuda() for b in bufs]
+    out = torch.full((w.coll_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    p = c3.Problem(dA, dB, dC, w.M, w.N, w.K, c3.C3_COLL_ALLREDUCE, out, w.unit_bytes, w.nranks, shards=dins)
+    t = c3.c3_run(p, mode, split, 0)
+    assert t["status"] == 0
+    assert t["smid_overlap"] == 0, t
+    ref = oracle.allreduce(bufs)[0].reshape(-1)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    rows = np.array([0, 1, w.M // 2, w.M - 1])
+    C_ref, S_ref = oracle.gemm(A[rows], B)
+    assert_gemm_close(dC[torch.from_numpy(rows).cuda()].cpu().numpy(), C_ref, S_ref)
+
+
 @pytest.mark.parametrize("wname", ["ffn70_ag", "l405_a2a", "mem_ar"])
 @pytest.mark.parametrize("engine", [0, 1])
 def test_collective_full_size_bit_exact(c3, wname, engine):
