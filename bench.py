@@ -143,7 +143,8 @@ def parse_args(argv=None):
     ap.add_argument("--heuristics", action="store_true",
                     help="instead of the headline line: calibrate the SM-split slowdown table once, then compare the "
                          "split the pages' heuristic predicts with the swept best over the size sweep")
-    ap.add_argument("--profile-range", choices=["gemm", "baseline", "ce", "sm_only", "ce_only", "ce_parallel_only"],
+    ap.add_argument("--profile-range", choices=["gemm", "baseline", "ce", "sm_only", "ce_only", "ce_parallel_only",
+                                                "ce_staged_only"],
                     default=None,
                     help="instead of the headline line: run one phase (the GEMM alone, or the GEMM concurrent with "
                          "the SM collective / the driver memcpy; or the collective alone on either) between cudaProfilerStart and "
@@ -911,11 +912,15 @@ def main(argv=None):
         torch.cuda.synchronize(dev)
         only = {"sm_only": (c3.C3_MODE_SERIAL_SM, c3.C3_CE_GRAPH),
                 "ce_only": (c3.C3_MODE_SERIAL_CE, ce_variant_arg(args, c3)),
-                "ce_parallel_only": (c3.C3_MODE_SERIAL_CE, c3.C3_CE_GRAPH_PARALLEL)}.get(args.profile_range)
+                "ce_parallel_only": (c3.C3_MODE_SERIAL_CE, c3.C3_CE_GRAPH_PARALLEL),
+                "ce_staged_only": (c3.C3_MODE_SERIAL_CE, c3.C3_CE_HOST_STAGED)}.get(args.profile_range)
         if only:
-            # the collective alone (an empty GEMM), so the range holds nothing else
+            # the collective alone (an empty GEMM), so the range holds nothing else; the
+            # host-staged variant bounces through a page-locked buffer of the copies' size
+            bounce = (torch.empty(w.coll_bytes, dtype=torch.uint8).pin_memory()
+                      if only[1] == c3.C3_CE_HOST_STAGED else None)
             cprob = c3.Problem(None, None, None, 0, 0, 0, coll_id, out, w.unit_bytes, w.nranks, shards=dshards,
-                               send=dsend, stream=stream, ce_variant=only[1])
+                               send=dsend, stream=stream, ce_variant=only[1], ce_stage=bounce)
             c3.c3_run(cprob, only[0], 0, 0)   # builds and caches the graph outside the range
             torch.cuda.synchronize(dev)
         torch.cuda.profiler.start()
