@@ -357,14 +357,16 @@ __global__ void __launch_bounds__(kVecThreads, 2) reduce_scatter_kernel(RsTable 
 // cover every slice, also on up to four fixed rounds of copy pieces.  The rest
 // is claimed from the group's counter, slices first, then pieces: up to eight
 // slices or four pieces a claim, fewer when the group's warps would otherwise
-// not get a claim each (a small all-reduce spreads over them).  So every sum slice is held by a warp that
-// does it before anything it might wait for, and the kernel always completes.
-// Finished slices are added to their chunk's count in the work slot (once per
-// chunk per claim, after every lane has fenced its stores); a copy piece of
-// chunk c first waits until that count is complete (acquire loads, bounded by
-// kWaitLimitNs; past it, or once another wait has given up, the piece is
-// skipped and the error recorded).  Being one launch group, a partitioned
-// all-reduce widens onto the SMs a GEMM leaves, as the copies do.
+// not get a claim each (a small all-reduce spreads over them).  So every sum
+// slice is held by a warp that does it before anything it might wait for, and
+// the kernel always completes.  Finished slices are added to their chunk's
+// count in the work slot (once per chunk per claim, after every lane has
+// fenced its stores); a copy piece of chunk c first waits until that count is
+// complete (acquire loads, bounded by kWaitLimitNs; past it, or once another
+// wait has given up, the piece is skipped and the error recorded).  Being one
+// launch group, a partitioned all-reduce widens onto the SMs a GEMM leaves, as
+// the copies do.  One 512-thread CTA fills an SM's registers (up to 128 a
+// thread): it runs only in partitions, whose CTAs hold their SMs alone anyway.
 constexpr uint64_t kArSlice = 32;   // vectors a sum slice (one a lane)
 constexpr unsigned kArClaim = 8;    // most sum slices a claim
 
