@@ -1090,7 +1090,7 @@ def main(argv=None):
         gbs = w.coll_traffic_bytes / tc_sm / 1e9
         copy_roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"],
-                     "kernel": ("reduce_scatter_kernel + copy_vec_kernel" if w.coll == "allreduce"
+                     "kernel": ("allreduce_push_kernel" if w.coll == "allreduce"
                                 else "copy_vec_kernel") + " (default budget)"}
         if w.coll_traffic_bytes < l2_bytes:
             copy_roof["regime"] = (f"launch-latency bound: the collective moves {w.coll_traffic_bytes / 1e6:.1f} MB, "

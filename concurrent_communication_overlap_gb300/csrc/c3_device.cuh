@@ -26,7 +26,6 @@ enum WaitSite : int {
     kSiteBulkLoad = 5,
     kSiteBulkDrain = 6,
     kSiteSelfTest = 7,
-    kSiteArChunk = 8,  // an all-reduce's all-gather piece waiting for its chunk's sums
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {

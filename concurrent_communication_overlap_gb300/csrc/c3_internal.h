@@ -19,9 +19,6 @@ struct CtaRec {
 constexpr int kCtaRecs = 256;      // CTAs recorded per kernel (the first 256)
 constexpr int kSchedSlots = 64;    // GEMM tile-scheduler counters, used round-robin by launches
 constexpr int kMaxRanksAr = 8;     // ranks of an all-reduce
-// Words of one SM-collective work slot: the next unit, the CTAs done, and per
-// all-reduce chunk the reduce-scatter pieces finished.
-constexpr int kCollSlotWords = 2 + kMaxRanksAr;
 
 // Device status block (library-owned, reset before each timed run).
 struct DevStatus {
@@ -44,11 +41,10 @@ struct DevStatus {
     // using a slot).
     unsigned int sched[kSchedSlots][2];
     // Work counters of the SM collective kernels, the same way: per slot, the
-    // next work unit and the number of CTAs done, then (all-reduce) per chunk
-    // the reduce-scatter pieces finished.  One slot serves a launch group --
-    // one launch, or several on different streams that share the collective's
-    // work -- and its last CTA puts the slot back to zero.
-    unsigned int coll_sched[kSchedSlots][kCollSlotWords];
+    // next work unit and the number of CTAs done.  One slot serves a launch
+    // group -- one launch, or several on different streams that share the
+    // collective's work -- and its last CTA puts the slot back to zero.
+    unsigned int coll_sched[kSchedSlots][2];
 };
 
 constexpr size_t kStatusBytes = 16384;
@@ -109,7 +105,6 @@ struct DeviceState {
     DevStatus* status = nullptr;       // device status block
     unsigned int next_sched = 0;       // round-robin scheduler slot
     unsigned int next_coll_sched = 0;  // round-robin copy work-counter slot
-    cudaStream_t s_comm_b = nullptr;   // second collective stream: the CTAs that wait for the GEMM's SMs
     bool ready = false;
 };
 
@@ -177,13 +172,13 @@ bool copy_units_fit(const SegTable& t);
 int copy_init_device(int max_reserve);
 int reduce_scatter_launch(const RsTable& t, int ctas, int smem_reserve, cudaStream_t s, DevStatus* st,
                           int* ctas_out);
-// The whole all-reduce on SMs (reduce-scatter `r` and the all-gather `t` of
-// its chunks) as one launch of a launch group, the group's counters as for
-// copy_sm_launch: `ctas` CTAs numbered from cta_base; gate_need and dependent
-// as for copy_sm_launch.
-int allreduce_sm_launch(const RsTable& r, const SegTable& t, int ctas, int cta_base, const CopyGroup& g,
-                        int smem_reserve, int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out,
-                        unsigned gate_need = 0, bool dependent = false);
+// The whole all-reduce `r` on SMs in one pass (each sum computed once and
+// stored into every rank's row), as one launch of a launch group, the group's
+// counter as for copy_sm_launch: `ctas` CTAs numbered from cta_base;
+// gate_need and dependent as for copy_sm_launch.
+int allreduce_sm_launch(const RsTable& r, int ctas, int cta_base, const CopyGroup& g, int smem_reserve,
+                        int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need = 0,
+                        bool dependent = false);
 int bulk_copy_smem_bytes();
 
 // `stage`: the page-locked host bounce buffer of kCeHostStaged (at least

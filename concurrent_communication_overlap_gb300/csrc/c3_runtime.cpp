@@ -82,7 +82,6 @@ static int init_device(DeviceState& ds, int dev) {
     C3_TRY(cudaDeviceGetStreamPriorityRange(&lo, &hi), "stream priority range");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_hi, cudaStreamNonBlocking, hi), "stream");
-    C3_TRY(cudaStreamCreateWithPriority(&ds.s_comm_b, cudaStreamNonBlocking, lo), "stream");
     C3_TRY(cudaStreamCreateWithFlags(&ds.s_capture, cudaStreamNonBlocking), "stream");
     for (auto& ev : ds.ev) C3_TRY(cudaEventCreate(&ev), "event");
     if (take_fault(kFaultDeviceInit))
@@ -101,7 +100,6 @@ static int init_device(DeviceState& ds, int dev) {
 static void release_device(DeviceState& ds) {
     if (ds.s_comm) cudaStreamDestroy(ds.s_comm);
     if (ds.s_comm_hi) cudaStreamDestroy(ds.s_comm_hi);
-    if (ds.s_comm_b) cudaStreamDestroy(ds.s_comm_b);
     if (ds.s_capture) cudaStreamDestroy(ds.s_capture);
     if (ds.device >= 0) ce_release_graphs(ds.device);
     for (auto& ev : ds.ev)
@@ -323,24 +321,13 @@ static int pick_flavour(const SegTable& t, int sm_kernel, bool exclusive) {
            : (exclusive && !t.host_src ? kSmkBulk : kSmkVec);
 }
 
-// A partitioned all-reduce on the SM engine (a launch group split in two
-// parts) runs on the fused all-reduce kernel: sums and copies claimed from
-// one counter, so the whole all-reduce widens onto the SMs a GEMM leaves.
-// Every other all-reduce -- unsplit, on the copy engine, or with the bulk
-// copy kernel asked for -- runs as the reduce-scatter kernel followed by the
-// copies (two launches, each over its whole grid at once: the faster form
-// when nothing has to widen).
-static bool ar_fused(const CollPlan& cp, int engine, int sm_kernel, bool split) {
-    return cp.has_rs && engine == C3_ENGINE_SM && sm_kernel != C3_SMK_BULK && split;
-}
-
 // One collective launch.  SM engine: `budget` CTAs (0 = default), one launch
 // group; exclusive = the CTAs keep their SMs to themselves (partitioning).
 // With `split_total` > budget the collective is the first part of a split
-// group of split_total CTAs (launch_coll_rest launches the others): an
-// all-reduce then runs on the fused kernel, or, with the bulk copy kernel,
-// its reduce-scatter records ds.ev[7], which the rest waits for.  *group
-// receives the group (SM engine).
+// group of split_total CTAs (launch_coll_rest launches the others).  *group
+// receives the group (SM engine).  An all-reduce on the SM engine runs as one
+// pass of its own kernel, whatever p->sm_kernel asks for the copies; on the
+// copy engine, as the reduce-scatter kernel and then memcpy of its chunks.
 static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_kernel, int l2_stream, int ce_variant,
                        int budget, bool exclusive, cudaStream_t s, int* ctas, int split_total = 0,
                        CopyGroup* group = nullptr) {
@@ -351,29 +338,18 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
     const int total = split_total > k ? split_total : k;
     if (engine == C3_ENGINE_SM && t.host_src && sm_kernel == C3_SMK_BULK)
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only; host sources take the vector kernel");
-    if (ar_fused(cp, engine, sm_kernel, split_total > k)) {
-        // the whole all-reduce in one launch group (its rest from launch_coll_rest)
-        CopyGroup g = copy_group(ds, total, k);
-        if (group) *group = g;
-        return allreduce_sm_launch(cp.rs, t, k, 0, g, exclusive ? exclusive_reserve(ds) : 0, l2_stream, s, ds.status,
-                                   ctas);
-    }
     if (cp.has_rs) {
-        // the reduce-scatter needs arithmetic: always SMs, whatever the engine
-        int rc = reduce_scatter_launch(cp.rs, k, exclusive ? exclusive_reserve(ds) : 0, s, ds.status, ctas);
-        if (rc) return rc;
-        if (split_total > k) {
-            cudaError_t e = cudaEventRecord(ds.ev[7], s);
-            if (e != cudaSuccess) return set_cuda_error(e, "event record");
+        if (engine == C3_ENGINE_SM) {
+            CopyGroup g = copy_group(ds, total, k);
+            if (group) *group = g;
+            return allreduce_sm_launch(cp.rs, k, 0, g, exclusive ? exclusive_reserve(ds) : 0, l2_stream, s,
+                                       ds.status, ctas);
         }
+        // the reduce-scatter needs arithmetic, so it runs on SMs; the copy engine carries the all-gather
+        int rc = reduce_scatter_launch(cp.rs, k, 0, s, ds.status, ctas);
+        if (rc) return rc;
         if (t.nseg == 0) return 0;
-        if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture, cp.stage);
-        const int flavour = pick_flavour(t, sm_kernel, exclusive);
-        const int reserve = (exclusive && flavour == kSmkVec) ? exclusive_reserve(ds) : 0;
-        CopyGroup g = copy_group(ds, total, k);
-        if (group) *group = g;
-        int dummy = 0;
-        return copy_sm_launch(t, k, 0, g, flavour, reserve, l2_stream, s, ds.status, &dummy);
+        return copy_ce_launch(t, ce_variant, s, ds.s_capture, cp.stage);
     }
     if (engine == C3_ENGINE_CE) return copy_ce_launch(t, ce_variant, s, ds.s_capture, cp.stage);
     const int flavour = pick_flavour(t, sm_kernel, exclusive);
@@ -387,28 +363,18 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
 // from `first`, exclusive like the first part, on stream `s2`.  Launched after
 // the GEMM, so its CTAs start only on SMs the GEMM has left: the collective
 // widens to them once the GEMM's CTAs finish (a CTA that finds no work left
-// exits at once).  An all-reduce on the fused kernel launches the rest of
-// that kernel's group; one run as the reduce-scatter kernel and copies has
-// its copies wait for the reduce-scatter launch.
-// `dependent`: s2 is the GEMM's stream and this launch directly follows the
-// GEMM there, as its programmatic dependent (not for the reduce-scatter
-// kernel's copies, which must also wait for that launch).
+// exits at once).  `dependent`: s2 is the GEMM's stream and this launch
+// directly follows the GEMM there, as its programmatic dependent.
 static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, int l2_stream, int first, int rest,
                             const CopyGroup& g, cudaStream_t s2, int* ctas, unsigned gemm_ctas,
                             bool dependent = false) {
     if (ctas) *ctas = 0;
     const SegTable& t = cp.seg;
     if (rest <= 0) return 0;
-    if (ar_fused(cp, C3_ENGINE_SM, sm_kernel, true))
-        return allreduce_sm_launch(cp.rs, t, rest, first, g, exclusive_reserve(ds), l2_stream, s2, ds.status, ctas,
+    if (cp.has_rs)
+        return allreduce_sm_launch(cp.rs, rest, first, g, exclusive_reserve(ds), l2_stream, s2, ds.status, ctas,
                                    gemm_ctas, dependent);
     if (t.nseg == 0 || t.seg_bytes == 0) return 0;
-    if (dependent && cp.has_rs)
-        return set_error(C3_EINVAL, "an all-reduce's copies after the reduce-scatter kernel cannot follow the GEMM directly");
-    if (cp.has_rs) {
-        cudaError_t e = cudaStreamWaitEvent(s2, ds.ev[7], 0);
-        if (e != cudaSuccess) return set_cuda_error(e, "wait for the reduce-scatter");
-    }
     const int flavour = pick_flavour(t, sm_kernel, true);
     const int reserve = flavour == kSmkVec ? exclusive_reserve(ds) : 0;
     return copy_sm_launch(t, rest, first, g, flavour, reserve, l2_stream, s2, ds.status, ctas, gemm_ctas, dependent);
@@ -418,7 +384,7 @@ static int launch_coll_rest(DeviceState& ds, const CollPlan& cp, int sm_kernel, 
 // its total, so its work counter would stay dirty: clear it behind the first
 // part, on the first part's stream.
 static void abandon_group(const CopyGroup& g, cudaStream_t s) {
-    if (g.work) cudaMemsetAsync(g.work, 0, kCollSlotWords * sizeof(unsigned int), s);
+    if (g.work) cudaMemsetAsync(g.work, 0, 2 * sizeof(unsigned int), s);
 }
 
 static int wait_event(cudaEvent_t ev, double limit_s) {
@@ -590,7 +556,6 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         return rc;
     }
     int gctas = 0, cctas = 0;
-    bool split_rest = false;  // the collective ran as a split launch group (second part on ds.ev[6])
     const bool serial = (mode == C3_MODE_SERIAL_SM || mode == C3_MODE_SERIAL_CE);
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
     // Host-side GEMM planning (tile choice, tensor maps) happens before the
@@ -647,27 +612,19 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
         // wait for the GEMM to finish.  The first part, which creates the
         // launch group, therefore goes out before the GEMM, and the GEMM's
         // completion event follows the second part: t_gemm_ev then covers
-        // the GEMM's stream (GEMM and the collective's second part).  An
-        // all-reduce on the fused kernel is such a group too (its copies wait
-        // for their chunk's sums inside the kernel).  One run as the
-        // reduce-scatter kernel and bulk copies must have its copies wait for
-        // the reduce-scatter launch: its second part keeps a stream of its own
-        // and the gemm_started gate.
+        // the GEMM's stream (GEMM and the collective's second part).  The
+        // all-reduce's one-pass kernel waits for nothing either, so it is
+        // split the same way.
         const bool part = (engine == C3_ENGINE_SM && sm_split > 0);
-        const bool dep_rest = part && (!t.has_rs || ar_fused(t, engine, p->sm_kernel, true));
         const int comm_budget = part ? sm_split : p->comm_sms;
-        cudaStream_t sc2 = ds.s_comm_b;
-        cudaEvent_t ev_c2 = ds.ev[6];
         CopyGroup grp;
         int cctas2 = 0;
         bool comm_launched = false, rest_launched = false;
-        if (part && !dep_rest && (e = cudaStreamWaitEvent(sc2, ev0, 0)) != cudaSuccess)
-            return set_cuda_error(e, "fork");
         // Each completion event is recorded right after its own launch(es), before
         // anything else is submitted.
         auto go_gemm = [&] {
             int r = gemm_enqueue(gl, sg, ds.status, &gctas);
-            if (r == C3_OK && dep_rest) {
+            if (r == C3_OK && part) {
                 r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sg,
                                      &cctas2, (unsigned)gctas, true);
                 rest_launched = (r == C3_OK);
@@ -682,15 +639,6 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
             if (r == C3_OK && (e = cudaEventRecord(ev_c, sc)) != cudaSuccess) r = set_cuda_error(e, "event record");
             return r;
         };
-        auto go_rest = [&] {
-            if (!part || dep_rest) return (int)C3_OK;
-            // gated on the GEMM: its CTAs leave at once while GEMM CTAs still wait for SMs
-            int r = launch_coll_rest(ds, t, p->sm_kernel, p->coll_l2, comm_budget, ds.sm_count - comm_budget, grp, sc2,
-                                     &cctas2, (unsigned)gctas);
-            rest_launched = (r == C3_OK);
-            if (r == C3_OK && (e = cudaEventRecord(ev_c2, sc2)) != cudaSuccess) r = set_cuda_error(e, "event record");
-            return r;
-        };
         // A failure after the collective went out still orders the caller's
         // stream after it, so that the caller may reuse its buffers once its
         // own stream has drained; a split group missing its second part has
@@ -700,30 +648,22 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
                 if (part && !rest_launched) abandon_group(grp, sc);
                 if (cudaEventRecord(ev_c, sc) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c, 0);
             }
-            if (rest_launched && !dep_rest && cudaEventRecord(ev_c2, sc2) == cudaSuccess) cudaStreamWaitEvent(s0, ev_c2, 0);
             return code;
         };
-        if (priority || reclaim || dep_rest) {
+        if (priority || reclaim || part) {
             if ((rc = go_comm())) return fail(rc);
             if ((rc = go_gemm())) return fail(rc);
         } else {
             if ((rc = go_gemm())) return rc;
             if ((rc = go_comm())) return fail(rc);
         }
-        if ((rc = go_rest())) return fail(rc);
         if ((e = cudaStreamWaitEvent(s0, ev_c, 0)) != cudaSuccess) return set_cuda_error(e, "join");
-        if (part && !dep_rest && (e = cudaStreamWaitEvent(s0, ev_c2, 0)) != cudaSuccess) return set_cuda_error(e, "join");
-        split_rest = part && !dep_rest;
         cctas += cctas2;
     }
     if ((e = cudaEventRecord(ev_end, s0)) != cudaSuccess) return set_cuda_error(e, "event record");
     if ((rc = wait_event(ev_end, 120.0))) return rc;
     out->t_gemm_ev = elapsed_s(ev0, ev_g);
     out->t_comm_ev = elapsed_s(ev0, ev_c);
-    if (split_rest) {
-        const double t2 = elapsed_s(ev0, ds.ev[6]);
-        if (t2 > out->t_comm_ev) out->t_comm_ev = t2;
-    }
     // From the start event to the later of the two completion events, each
     // recorded right after its kernel(s), as the isolated phases are timed;
     // the join that orders the caller's stream after both is not part of it.

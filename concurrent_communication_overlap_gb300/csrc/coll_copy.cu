@@ -77,12 +77,10 @@ __device__ __forceinline__ bool gate_closed(const DevStatus* st, unsigned gate_n
 }
 
 // The last CTA of a launch group to finish puts the group's work counter back
-// to zero (and the `extra` words after the two counters: an all-reduce's
-// per-chunk counts), so the slot is clean for its next user.
-__device__ __forceinline__ void group_done(unsigned int* work, int total_ctas, int extra = 0) {
+// to zero, so the slot is clean for its next user.
+__device__ __forceinline__ void group_done(unsigned int* work, int total_ctas) {
     __threadfence();
     if (atomicAdd(&work[1], 1u) == (unsigned)total_ctas - 1u) {
-        for (int i = 0; i < extra; ++i) atomicExch(&work[2 + i], 0u);
         atomicExch(&work[0], 0u);
         atomicExch(&work[1], 0u);
     }
@@ -344,31 +342,23 @@ __global__ void __launch_bounds__(kVecThreads, 2) reduce_scatter_kernel(RsTable 
     if (threadIdx.x == 0) stamp_end(st, false);
 }
 
-// The whole all-reduce on SMs as one launch group.  Its work comes in two
-// kinds of unit:
-//   sum slices -- 32 16-byte vectors of one chunk c (one a lane): each element
-//       the rank-order fp32 sum (0 + in_0[i]) + in_1[i] + ..., all ranks'
-//       loads in flight at once, written into rank c's row (as
-//       reduce_scatter_kernel does);
-//   copy pieces -- the copy kernel's 4 KiB pieces of the segments "chunk c of
-//       row c -> row r" (chunk-major).
-// The first part's warps start on fixed sum slices, one each (interleaved
-// across its CTAs, so a small all-reduce spreads over every warp); when those
-// cover every slice, also on up to four fixed rounds of copy pieces.  The rest
-// is claimed from the group's counter, slices first, then pieces: up to eight
-// slices or four pieces a claim, fewer when the group's warps would otherwise
-// not get a claim each (a small all-reduce spreads over them).  So every sum
-// slice is held by a warp that does it before anything it might wait for, and
-// the kernel always completes.  Finished slices are added to their chunk's
-// count in the work slot (once per chunk per claim, after every lane has
-// fenced its stores); a copy piece of chunk c first waits until that count is
-// complete (acquire loads, bounded by kWaitLimitNs; past it, or once another
-// wait has given up, the piece is skipped and the error recorded).  Being one
-// launch group, a partitioned all-reduce widens onto the SMs a GEMM leaves, as
-// the copies do.  One 512-thread CTA fills an SM's registers (up to 128 a
-// thread): it runs only in partitions, whose CTAs hold their SMs alone anyway.
-constexpr uint64_t kArSlice = 32;   // vectors a sum slice (one a lane)
-constexpr unsigned kArClaim = 8;    // most sum slices a claim
+// The whole all-reduce on SMs in one pass: every 16-byte vector of the sum is
+// computed once -- the rank-order fp32 sum (0 + in_0[i]) + in_1[i] + ...,
+// all ranks' loads in flight at once -- and stored into every rank's row.  So
+// each input byte is read once and each output byte written once, the least an
+// all-reduce of R vectors inside one HBM moves: R + R vectors' worth, against
+// (R + 1) + 2 (R - 1) for a reduce-scatter followed by copies of its chunks.
+// (The pages split the all-reduce in two to hand the all-gather half to DMA
+// engines; the copy-engine path keeps that split.)  The result is the same bit
+// for bit on every row.  The work is a list of slices of 32 vectors (one a
+// lane), dealt and claimed the way the copy kernel deals its pieces: the first
+// part's warps start on up to four fixed rounds of slices (interleaved across
+// its CTAs, so a small all-reduce spreads over every SM of the part), the rest
+// are claimed from the group's counter eight at a time (fewer when the group's
+// warps would otherwise not get a claim each).  Nothing waits on anything, so
+// a partitioned all-reduce widens onto the SMs a GEMM leaves, as the copies do.
+constexpr uint64_t kArSlice = 32;   // vectors a slice (one a lane)
+constexpr unsigned kArClaim = 8;    // most slices a claim
 
 // units a claim: `most`, or fewer so that `units` make at least one claim a warp of the group
 __device__ __forceinline__ uint32_t claim_size(uint32_t units, unsigned most, int total_ctas) {
@@ -376,136 +366,73 @@ __device__ __forceinline__ uint32_t claim_size(uint32_t units, unsigned most, in
     return per < 1u ? 1u : per > most ? most : per;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned int* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 template <bool kStream>
-__global__ void __launch_bounds__(kVecThreads, 1)
-    allreduce_vec_kernel(RsTable r, SegTable t, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
-                         unsigned static_units, unsigned gate_need) {
+__global__ void __launch_bounds__(kVecThreads, 2)
+    allreduce_push_kernel(RsTable r, DevStatus* st, unsigned int* work, int cta_base, int total_ctas,
+                          unsigned static_units, unsigned gate_need) {
     const unsigned long long t_enter = globaltimer();
     if (gate_closed(st, gate_need)) {
-        if (threadIdx.x == 0) group_done(work, total_ctas, kMaxRanksAr);
+        if (threadIdx.x == 0) group_done(work, total_ctas);
         return;
     }
     const int lane = threadIdx.x & 31;
     const uint64_t pol = kStream ? policy_evict_first() : 0;
-    const uint64_t chunk_vecs = r.chunk >> 2;  // 16-byte vectors of a chunk (and of a copy segment)
-    // unit counts fit in 32 bits (allreduce_sm_launch bounds them)
-    const uint32_t spc = (uint32_t)((chunk_vecs + kArSlice - 1) / kArSlice);  // sum slices a chunk
-    const uint32_t ppc = (uint32_t)((chunk_vecs + kVecPiece - 1) / kVecPiece); // copy pieces a segment
-    const uint32_t slices = spc * (uint32_t)r.nranks;
-    const uint32_t pieces = ppc * (uint32_t)t.nseg;
-    const uint32_t segs_per_chunk = r.nranks > 1 ? (uint32_t)r.nranks - 1u : 1u;
-    unsigned int* const chunk_done = work + 2;
-
-    // one sum slice; returns its chunk
-    auto sum_slice = [&](uint32_t sl) -> uint32_t {
-        const uint32_t c = sl / spc;
-        const uint64_t v = (uint64_t)c * chunk_vecs + (uint64_t)(sl - c * spc) * kArSlice + (uint64_t)lane;
-        if (v < (uint64_t)(c + 1) * chunk_vecs) {
-            uint4 x[kMaxRanksAr];
+    const uint64_t nvec = r.count >> 2;  // 16-byte vectors of a rank's vector
+    // slice counts fit in 32 bits (allreduce_sm_launch bounds them)
+    const uint32_t slices = (uint32_t)((nvec + kArSlice - 1) / kArSlice);
+    auto slice = [&](uint32_t sl) {
+        const uint64_t v = (uint64_t)sl * kArSlice + (uint64_t)lane;
+        if (v >= nvec) return;
+        uint4 x[kMaxRanksAr];
 #pragma unroll
-            for (int q = 0; q < kMaxRanksAr; ++q)
-                if (q < r.nranks) {
-                    const uint8_t* src = reinterpret_cast<const uint8_t*>(r.in[q]) + (v << 4);
-                    x[q] = kStream ? ld_vec_stream(src, pol) : ld_vec(src);
-                }
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < kMaxRanksAr; ++q)
-                if (q < r.nranks) {
-                    acc.x = __fadd_rn(acc.x, __uint_as_float(x[q].x));
-                    acc.y = __fadd_rn(acc.y, __uint_as_float(x[q].y));
-                    acc.z = __fadd_rn(acc.z, __uint_as_float(x[q].z));
-                    acc.w = __fadd_rn(acc.w, __uint_as_float(x[q].w));
-                }
-            // a normal store: the copies read it back from L2
-            reinterpret_cast<float4*>(r.out + (uint64_t)c * r.count)[v] = acc;
-        }
-        return c;
-    };
-    // adds n finished slices to chunk c's count, after every lane's stores
-    auto publish = [&](uint32_t c, unsigned n) {
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(&chunk_done[c], n);
-    };
-
-    unsigned ready = 0;    // chunks whose sums this warp has seen complete
-    bool gave_up = false;  // a wait of this warp ran out (or another's did): skip the rest
-    auto copy_piece = [&](uint32_t p) {
-        if (gave_up) return;
-        const uint32_t seg = p / ppc;
-        const uint32_t c = seg / segs_per_chunk;
-        if (!((ready >> c) & 1u)) {
-            const unsigned long long t0 = globaltimer();
-            for (;;) {
-                const unsigned d = ld_acquire_gpu(&chunk_done[c]);
-                if (__all_sync(0xffffffffu, d >= spc)) break;
-                int stop = 0;
-                if (lane == 0)
-                    stop = (globaltimer() - t0 > kWaitLimitNs) ||
-                           (st != nullptr && *reinterpret_cast<volatile int*>(&st->error) != 0);
-                if (__shfl_sync(0xffffffffu, stop, 0)) {
-                    if (lane == 0) report_error(st, -4, kSiteArChunk);
-                    gave_up = true;
-                    return;
-                }
-                __nanosleep(64);
+        for (int q = 0; q < kMaxRanksAr; ++q)
+            if (q < r.nranks) {
+                const uint8_t* in = reinterpret_cast<const uint8_t*>(r.in[q]) + (v << 4);
+                x[q] = kStream ? ld_vec_stream(in, pol) : ld_vec(in);
             }
-            ready |= 1u << c;
-        }
-        // the sums were written during this kernel: load them through L2 (.cg), not the read-only path
-        const uint64_t vbase = (uint64_t)(p - seg * ppc) * kVecPiece;
-        const uint8_t* src = t.src[seg] + ((vbase + (uint64_t)lane) << 4);
-        uint8_t* dst = t.dst[seg] + ((vbase + (uint64_t)lane) << 4);
-        uint4 v[kVecUnroll];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u)
-            if (vbase + (uint64_t)(u * 32 + lane) < chunk_vecs)
-                v[u] = __ldcg(reinterpret_cast<const uint4*>(src + u * 512));
+        for (int q = 0; q < kMaxRanksAr; ++q)
+            if (q < r.nranks) {
+                acc.x = __fadd_rn(acc.x, __uint_as_float(x[q].x));
+                acc.y = __fadd_rn(acc.y, __uint_as_float(x[q].y));
+                acc.z = __fadd_rn(acc.z, __uint_as_float(x[q].z));
+                acc.w = __fadd_rn(acc.w, __uint_as_float(x[q].w));
+            }
+        const uint4 a = make_uint4(__float_as_uint(acc.x), __float_as_uint(acc.y), __float_as_uint(acc.z),
+                                   __float_as_uint(acc.w));
 #pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u)
-            if (vbase + (uint64_t)(u * 32 + lane) < chunk_vecs) {
+        for (int q = 0; q < kMaxRanksAr; ++q)
+            if (q < r.nranks) {
+                uint8_t* out = reinterpret_cast<uint8_t*>(r.out + (uint64_t)q * r.count) + (v << 4);
                 if (kStream)
-                    st_vec_stream(dst + u * 512, v[u], pol);
+                    st_vec_stream(out, a, pol);
                 else
-                    st_vec(dst + u * 512, v[u]);
+                    st_vec(out, a);
             }
     };
 
     const unsigned cta = (unsigned)cta_base + blockIdx.x;
     const unsigned first_ctas = static_units / kVecWarps;  // CTAs of the first part
-    const unsigned warp_id = (unsigned)(threadIdx.x >> 5) * first_ctas + cta;  // fixed-unit index (first part)
-    const uint32_t fixed_slices = static_units < slices ? static_units : slices;
-    // fixed copy rounds only when the fixed slices are every slice (nothing a fixed copy waits for is claimed)
-    uint32_t fixed_pieces = 0;
-    if (fixed_slices == slices && static_units > 0) {
-        const uint32_t rounds = (pieces + static_units - 1) / static_units;
-        fixed_pieces = rounds < kVecClaim ? pieces : kVecClaim * static_units;
-    }
-    const uint32_t sc = claim_size(slices - fixed_slices, kArClaim, total_ctas);
-    const uint32_t pc = claim_size(pieces - fixed_pieces, kVecClaim, total_ctas);
-    const uint32_t slice_claims = (slices - fixed_slices + sc - 1) / sc;
-    const uint32_t claims = slice_claims + (pieces - fixed_pieces + pc - 1) / pc;
+    const uint64_t round = static_units;                     // slices a fixed round
+    const uint64_t rounds = round ? ((slices + round - 1) / round < kVecClaim ? (slices + round - 1) / round
+                                                                              : kVecClaim)
+                                  : 0;
+    const uint32_t fixed = (uint32_t)(rounds * round < slices ? rounds * round : slices);
+    const uint32_t sc = claim_size(slices - fixed, kArClaim, total_ctas);
+    const uint32_t claims = (slices - fixed + sc - 1) / sc;
     bool worked = false;
     if (cta < first_ctas) {
-        if (warp_id < fixed_slices) {
-            publish(sum_slice(warp_id), 1u);
-            worked = true;
-        }
 #pragma unroll 1
-        for (uint32_t p = warp_id; p < fixed_pieces; p += static_units) {
-            copy_piece(p);
-            worked = true;
+        for (uint64_t j = 0; j < rounds; ++j) {
+            const uint64_t sl = j * round + (uint64_t)(threadIdx.x >> 5) * first_ctas + cta;
+            if (sl < fixed) {
+                slice((uint32_t)sl);
+                worked = true;
+            }
         }
     }
-    // claim q: sum slices fixed_slices + sc q .. + sc - 1, or (past them) copy pieces
-    // fixed_pieces + pc (q - slice_claims) .. + pc - 1; lane 0 claims the warp's next while the current one runs
+    // claim q: slices fixed + sc q .. + sc - 1; lane 0 claims the warp's next while the current one runs
     unsigned q = claims;
     if (claims > 0) {
         unsigned c0 = 0;
@@ -516,33 +443,15 @@ __global__ void __launch_bounds__(kVecThreads, 1)
         worked = true;
         unsigned next = 0;
         if (lane == 0) next = atomicAdd(&work[0], 1u);
-        if (q < slice_claims) {
-            const uint32_t s0 = fixed_slices + q * sc;
-            uint32_t cur = ~0u;
-            unsigned n = 0;
+        const uint32_t s0 = fixed + q * sc;
 #pragma unroll 1
-            for (unsigned i = 0; i < sc && s0 + i < slices; ++i) {
-                const uint32_t c = sum_slice(s0 + i);
-                if (c != cur) {
-                    if (n) publish(cur, n);
-                    cur = c;
-                    n = 0;
-                }
-                ++n;
-            }
-            if (n) publish(cur, n);
-        } else {
-            const uint32_t a0 = fixed_pieces + (q - slice_claims) * pc;
-#pragma unroll 1
-            for (unsigned i = 0; i < pc; ++i)
-                if (a0 + i < pieces) copy_piece(a0 + i);
-        }
+        for (uint32_t i = 0; i < sc && s0 + i < slices; ++i) slice(s0 + i);
         q = __shfl_sync(0xffffffffu, next, 0);
     }
     const int cta_worked = __syncthreads_or(worked ? 1 : 0);
     if (threadIdx.x == 0) {
         if (cta_worked) stamp_window(st, false, cta, t_enter, globaltimer());
-        group_done(work, total_ctas, kMaxRanksAr);
+        group_done(work, total_ctas);
     }
 }
 
@@ -577,9 +486,9 @@ int copy_init_device(int max_reserve) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_reserve);
             if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(copy_vec_kernel)");
         }
-        for (auto fn : {allreduce_vec_kernel<false>, allreduce_vec_kernel<true>}) {
+        for (auto fn : {allreduce_push_kernel<false>, allreduce_push_kernel<true>}) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_reserve);
-            if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(allreduce_vec_kernel)");
+            if (e != cudaSuccess) return set_cuda_error(e, "cudaFuncSetAttribute(allreduce_push_kernel)");
         }
     }
     return 0;
@@ -652,26 +561,21 @@ int copy_sm_launch(const SegTable& t, int ctas, int cta_base, const CopyGroup& g
     return 0;
 }
 
-int allreduce_sm_launch(const RsTable& r, const SegTable& t, int ctas, int cta_base, const CopyGroup& g,
-                        int smem_reserve, int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out,
-                        unsigned gate_need, bool dependent) {
+int allreduce_sm_launch(const RsTable& r, int ctas, int cta_base, const CopyGroup& g, int smem_reserve,
+                        int l2_stream, cudaStream_t s, DevStatus* st, int* ctas_out, unsigned gate_need,
+                        bool dependent) {
     if (ctas_out) *ctas_out = 0;
     if (r.count == 0) return 0;
-    if (r.nranks < 1 || r.nranks > kMaxRanksAr || (r.chunk & 3u) || r.chunk * (uint64_t)r.nranks != r.count)
-        return set_error(-1, "all-reduce table is inconsistent");
-    if (t.nseg != r.nranks * (r.nranks - 1) || (t.nseg > 0 && t.seg_bytes != r.chunk * sizeof(float)))
-        return set_error(-1, "all-reduce copy table does not match its chunks");
+    if (r.nranks < 1 || r.nranks > kMaxRanksAr || (r.count & 3u)) return set_error(-1, "all-reduce table is inconsistent");
     if (!group_covers(g, ctas, cta_base)) return set_error(-1, "all-reduce launch group does not cover this launch");
-    // 512-byte sum slices and 4 KiB copy pieces: every unit count, and the claims past them, stay far inside 32 bits
-    const uint64_t spc = ((r.chunk >> 2) + kArSlice - 1) / kArSlice;
-    const uint64_t ppc = ((r.chunk >> 2) + kVecPiece - 1) / kVecPiece;
-    if (spc * (uint64_t)r.nranks + ppc * (uint64_t)t.nseg >= (1ull << 30))
-        return set_error(-5, "all-reduce has too many work units");
+    // 512-byte slices: the slice count, and the claims past it, stay far inside 32 bits
+    if (((r.count >> 2) + kArSlice - 1) / kArSlice >= (1ull << 30))
+        return set_error(-5, "all-reduce has too many 512-byte slices");
     if (take_fault(kFaultSmCollLaunch)) return set_error(-3, "injected failure: SM collective launch");
     if (ctas < 1) return set_error(-1, "all-reduce launch needs at least one CTA");
     const unsigned su = (unsigned)g.static_ctas * (unsigned)kVecWarps;
-    cudaError_t e = launch_part(l2_stream ? allreduce_vec_kernel<true> : allreduce_vec_kernel<false>, ctas,
-                                kVecThreads, smem_reserve, s, dependent, r, t, st, g.work, cta_base, g.total_ctas, su,
+    cudaError_t e = launch_part(l2_stream ? allreduce_push_kernel<true> : allreduce_push_kernel<false>, ctas,
+                                kVecThreads, smem_reserve, s, dependent, r, st, g.work, cta_base, g.total_ctas, su,
                                 gate_need);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_cuda_error(e, "all-reduce kernel launch");

@@ -161,12 +161,12 @@ class Workload:
     @property
     def coll_traffic_bytes(self) -> int:
         """Bytes the collective must read and write at least: 2x its size for
-        the copies; for the all-reduce, the reduce-scatter reads every rank's
-        vector and writes one, then the all-gather copies R-1 of R chunks to
-        every rank (read + write)."""
+        the copies; for the all-reduce, every rank's vector read once and every
+        rank's row written once (the SM engine's one pass moves exactly that;
+        the copy-engine form, a reduce-scatter and then copies of its chunks,
+        moves (3R - 1) rows)."""
         if self.coll == "allreduce":
-            row = self.unit_bytes
-            return (self.nranks + 1) * row + 2 * (self.nranks - 1) * row
+            return 2 * self.nranks * self.unit_bytes
         return 2 * self.coll_bytes
 
     @property

@@ -34,11 +34,9 @@
  *   - Streams are `cudaStream_t` values passed as `c3_stream` (void *); NULL
  *     means the legacy default stream.
  *   - The library owns a few internal objects per device, created on first use
- *     with that device current and released by c3_shutdown(): four CUDA
- *     streams (the forked collective's, the same at the highest priority, a
- *     second collective stream for the part of a partitioned collective that
- *     waits for the GEMM's SMs, and a private stream for capturing memcpy
- *     graphs), CUDA events, up to 16
+ *     with that device current and released by c3_shutdown(): three CUDA
+ *     streams (the forked collective's, the same at the highest priority, and
+ *     a private stream for capturing memcpy graphs), CUDA events, up to 16
  *     cached memcpy graphs, a 16 KiB device status block
  *     (error word, %globaltimer stamps, per-CTA %smid residency records) and
  *     the kernels' function attributes.
@@ -240,22 +238,25 @@ int c3_alltoall(const void *in, void *out, size_t block_bytes, int nranks, int e
                 int sm_budget, c3_stream s);
 
 /*
- * All-reduce of `nranks` fp32 vectors of `count` elements, decomposed the way
- * the pages propose for DMA offload: a reduce-scatter, which needs arithmetic
- * and always runs on SMs, then an all-gather of the reduced chunks, which
- * `engine` carries (C3_ENGINE_CE: driver memcpy; C3_ENGINE_SM: the SM copy
- * kernel) (synthesis page, "Attack 1"; pith.science paper page, "Reading
- * between the lines": a DMA engine has no arithmetic).
+ * All-reduce of `nranks` fp32 vectors of `count` elements.
+ *   engine C3_ENGINE_CE: decomposed the way the pages propose for DMA offload,
+ *     a reduce-scatter, which needs arithmetic and runs on SMs, then an
+ *     all-gather of the reduced chunks as driver memcpy (synthesis page,
+ *     "Attack 1"; pith.science paper page, "Reading between the lines": a DMA
+ *     engine has no arithmetic);
+ *   engine C3_ENGINE_SM: one pass on SMs.  Each 16-byte vector of the sum is
+ *     computed once and stored into every rank's row, so every input byte is
+ *     read once and every output byte written once (2 * nranks * count * 4
+ *     bytes; the reduce-scatter and copies of the copy-engine form move
+ *     (3 * nranks - 1) * count * 4).
  *   inputs  HOST array of nranks device pointers, count floats each, 16-byte aligned
  *   out     device, nranks * count floats: row r (out + r*count) is rank r's result
  *   count   multiple of 4 * nranks (16-byte chunks; else C3_EALIGN); 0 launches nothing
  *   nranks  1..8
  * Every row ends as out[r][i] = ((0 + in_0[i]) + in_1[i]) + ... + in_{R-1}[i]
- * in fp32, rank order -- the same on every row and bit-reproducible.  The
- * reduce-scatter uses sm_budget SMs (0 = default).  Asynchronous on `s`.
- * (A partitioned c3_run runs the all-reduce as one fused kernel; see c3_run.
- * A wait inside that kernel that gives up -- a copy waiting past the 2 s
- * limit for its chunk's sums -- is C3_ETIMEOUT, as for every bounded wait.)
+ * in fp32, rank order -- the same on every row, on either engine, and
+ * bit-reproducible.  The SM work (the one pass, or the reduce-scatter) uses
+ * sm_budget SMs (0 = default).  Asynchronous on `s`.
  */
 int c3_allreduce(const float *const *inputs, float *out, size_t count, int nranks, int engine,
                  int sm_budget, c3_stream s);
@@ -379,16 +380,8 @@ typedef struct {
  *   CTA waits for an SM, and they run only on SMs the GEMM has left -- a
  *   collective that outlasts the GEMM widens onto them.  t_gemm_ev then times
  *   the GEMM's stream, the GEMM and that second part.  An all-reduce on the
- *   SM engine is such a group too: in both partitioned modes it runs as one
- *   fused kernel whose warps claim the reduce-scatter's sums and then the
- *   all-gather's copies from one counter, a copy of a chunk waiting in the
- *   kernel until that chunk's sums are all written, so the whole all-reduce
- *   widens.  With p->sm_kernel == C3_SMK_BULK it keeps the reduce-scatter
- *   kernel and bulk copies: the copies must wait for the reduce-scatter
- *   launch, so their rest goes on another library stream and is gated instead
- *   (a CTA that starts while GEMM CTAs have not all started leaves at once,
- *   and the collective may then not widen).  The result is bit-identical
- *   either way.
+ *   SM engine is such a group too: its one-pass kernel (see c3_allreduce)
+ *   waits for nothing, so the whole all-reduce widens.
  *   mode C3_MODE_SERIAL_SM / _CE: GEMM then collective on one stream.
  * Fills t_conc, the device windows, CTA counts and %smid facts of `out`; the
  * fields marked (c3_time) are left 0.  Returns C3_OK, an argument error

@@ -153,10 +153,10 @@ def test_partitioned_collective_widens_onto_the_sms_the_gemm_leaves(c3, mode, pr
 @pytest.mark.parametrize("mode,prio", [(1, 0), (1, 1), (4, 0)])
 def test_partitioned_allreduce_widens_onto_the_sms_the_gemm_leaves(c3, mode, prio):
     """The same one-tile GEMM beside an all-reduce of eight 8 M-element fp32
-    vectors partitioned onto 8 SMs: the fused all-reduce kernel is one launch
-    group, so its second part takes the SMs the GEMM leaves for both halves
-    (the sums and the copies of each chunk); the output is the oracle's
-    rank-order sum bit for bit and no SM holds both kernels at once."""
+    vectors partitioned onto 8 SMs: the all-reduce's one-pass kernel is one
+    launch group, so its second part takes the SMs the GEMM leaves; the output
+    is the oracle's rank-order sum bit for bit and no SM holds both kernels at
+    once."""
     info = c3.c3_get_device_info()
     M, N, K = 128, 128, 64
     A = I.bf16_uniform(23, (M, K))
@@ -177,7 +177,7 @@ def test_partitioned_allreduce_widens_onto_the_sms_the_gemm_leaves(c3, mode, pri
     assert (np.abs(dC.cpu().numpy().astype(np.float64) - C_ref) <= TOL * S_ref).all()
     assert t["smid_overlap"] == 0, t
     assert t["comm_ctas"] == info["sm_count"]
-    # 8 SMs alone would need ~1 ms for its ~0.8 GB of traffic; the idle SMs join at once
+    # 8 SMs alone would need ~0.7 ms for its ~0.5 GB of traffic; the idle SMs join at once
     assert t["comm_sms"] > 64, t
 
 
@@ -193,10 +193,9 @@ def _tiny_gemm(seed):
 
 def test_partitioned_allreduce_work_counters_recycle_over_many_launches(c3):
     """More partitioned all-reduce runs than work slots (64), with first parts
-    of 1..7 SMs (most sum slices claimed) and of 12..32 SMs (every slice a
-    fixed unit, the copies in fixed rounds), and a poisoned output each time:
-    a claim counter left non-zero would skip units, and a chunk count left
-    non-zero would let the copies run ahead of the sums (copying the poison)."""
+    of 1..7 SMs (most slices claimed from the counter) and of 12..32 SMs (every
+    slice a fixed unit), and a poisoned output each time: a claim counter left
+    non-zero would skip slices and leave the poison in place."""
     (M, N, K), _, (dA, dB, dC) = _tiny_gemm(31)
     R, count = 8, 8 * 3000 + 32          # 3004 elements a chunk: ragged slices and pieces
     bufs = [I.normal(1200 + r, count).astype(np.float32) for r in range(R)]
@@ -218,9 +217,9 @@ def test_partitioned_allreduce_work_counters_recycle_over_many_launches(c3):
 @pytest.mark.parametrize("split", [8, 64])
 @pytest.mark.parametrize("l2", [0, 1])   # normal, evict-first loads and stores
 def test_partitioned_allreduce_bit_exact(c3, nranks, count, split, l2):
-    """The fused all-reduce kernel (partitioned runs) at rank counts 1..8 and
-    ragged chunks, with either L2 policy, against the oracle's rank-order fp32
-    sum."""
+    """The all-reduce's one-pass kernel in partitioned runs at rank counts 1..8
+    and ragged sizes, with either L2 policy, against the oracle's rank-order
+    fp32 sum."""
     (M, N, K), (A, B), (dA, dB, dC) = _tiny_gemm(41)
     bufs = [I.normal(1300 + r, count).astype(np.float32) for r in range(nranks)]
     bufs[0][:3] = [-0.0, np.inf, 1e38]

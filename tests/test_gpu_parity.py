@@ -247,7 +247,7 @@ def test_allreduce_bit_exact(c3, engine, nranks, count):
 @pytest.mark.parametrize("mode,split,prio,flavour", [
     (1, 0, 0, 0), (1, 0, 1, 0), (1, 16, 0, 0), (1, 16, 1, 0), (4, 16, 0, 0), (2, 0, 0, 0), (2, 8, 0, 0),
     (0, 0, 0, 0), (3, 0, 0, 0),
-    # the bulk copy kernel: reduce-scatter kernel, then the copies (gated second part)
+    # the bulk copy flavour asked for: the all-reduce keeps its own one-pass kernel
     (1, 0, 0, 2), (1, 16, 0, 2), (4, 16, 0, 2)])
 @pytest.mark.parametrize("variant", [0, 2, 4])
 def test_allreduce_in_every_mode(c3, mode, split, prio, flavour, variant):
@@ -303,8 +303,8 @@ def test_gemm_full_size_compute_bound_rows_and_columns(c3, wname):
 @pytest.mark.parametrize("mode,split", [(1, 32), (4, 16)])
 def test_allreduce_full_size_partitioned(c3, mode, split):
     """The memory-bound all-reduce pair at full size in a partitioned and a
-    reclaim run (the fused all-reduce kernel beside the HBM-bound GEMM): the
-    all-reduce bit-exact against the oracle, sampled GEMM rows within the
+    reclaim run (the all-reduce's one-pass kernel beside the HBM-bound GEMM):
+    the all-reduce bit-exact against the oracle, sampled GEMM rows within the
     tolerance."""
     w = I.WORKLOADS["mem_ar"]
     A, B = I.gemm_operands(w)
