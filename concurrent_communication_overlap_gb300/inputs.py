@@ -199,7 +199,7 @@ WORKLOADS = {
     "mem_ar": Workload("mem_ar", 256, 28672, 8192, ("normal", 0.0, 1.0), ("normal", 0.0, 0.02),
                        "allreduce", 8, 16 * MiB, "f32normal",
                        "memory-bound bf16 GEMM 256x28672x8192 with an 8-rank all-reduce of 8 x 16 MiB fp32 "
-                       "gradients (reduce-scatter on SMs, all-gather on the mode's engine)"),
+                       "gradients (one pass on SMs; on the copy engine a reduce-scatter on SMs, then memcpy)"),
     "l405_a2a": Workload("l405_a2a", 8192, 53248, 16384, ("normal", 0.0, 1.0), ("normal", 0.0, 0.02),
                          "alltoall", 8, 8 * MiB, "u16",
                          "Llama-405B-shaped bf16 GEMM 8192x53248x16384 with an 8x8 all-to-all of "
