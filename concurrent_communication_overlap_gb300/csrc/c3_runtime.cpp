@@ -340,9 +340,17 @@ static int launch_coll(DeviceState& ds, const CollPlan& cp, int engine, int sm_k
         return set_error(C3_EUNSUP, "the bulk copy kernel reads device memory only; host sources take the vector kernel");
     if (cp.has_rs) {
         if (engine == C3_ENGINE_SM) {
-            CopyGroup g = copy_group(ds, total, k);
+            // On the default budget (every SM), an unpartitioned all-reduce that moves
+            // less than 512 MiB runs two CTAs an SM: more loads in flight through its
+            // ramp and tail (16 MiB a rank: 42.6 us against 46.7 on one an SM).  Larger
+            // ones keep one (64 MiB a rank: 161.5 against 167.6 us; one CTA an SM
+            // already streams at the HBM rate there).  A budget the caller sets is kept.
+            const uint64_t traffic = 2ull * (uint64_t)cp.rs.nranks * cp.rs.count * sizeof(float);
+            const bool twice = budget <= 0 && !exclusive && split_total <= k && traffic < (512ull << 20);
+            const int kk = twice ? 2 * k : k;
+            CopyGroup g = copy_group(ds, split_total > k ? total : kk, kk);
             if (group) *group = g;
-            return allreduce_sm_launch(cp.rs, k, 0, g, exclusive ? exclusive_reserve(ds) : 0, l2_stream, s,
+            return allreduce_sm_launch(cp.rs, kk, 0, g, exclusive ? exclusive_reserve(ds) : 0, l2_stream, s,
                                        ds.status, ctas);
         }
         // the reduce-scatter needs arithmetic, so it runs on SMs; the copy engine carries the all-gather
