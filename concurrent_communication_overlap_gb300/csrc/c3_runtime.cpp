@@ -568,11 +568,20 @@ static int run_once(DeviceState& ds, const c3_problem* p, const CollPlan& t, int
     const int engine = (mode == C3_MODE_CONCURRENT_CE || mode == C3_MODE_SERIAL_CE) ? C3_ENGINE_CE : C3_ENGINE_SM;
     // Host-side GEMM planning (tile choice, tensor maps) happens before the
     // start event: only device work and launch calls are timed.
-    const int gemm_cap = (!serial && sm_split > 0 && !reclaim_mode) ? ds.sm_count - sm_split : 0;
+    // A partition caps the GEMM at SM count - sm_split.  With reclaim its tiles are
+    // planned for those SMs too, the ones it starts on, but it is launched on up to
+    // every SM: CTAs that find their SM held start late, as the collective's SMs
+    // free up, and take whatever tiles are left.  A GEMM whose tiles fit one wave
+    // on the SMs it starts on then leaves none for a late second wave.  Every tile,
+    // the first included, is claimed from the counter.
+    const int gemm_cap = (!serial && sm_split > 0) ? ds.sm_count - sm_split : 0;
     GemmLaunch gl;
     if ((rc = gemm_prepare(p->A, p->B, p->C, p->M, p->N, p->K, gemm_cap, &gl))) return rc;
-    // with reclaim, CTAs that find their SM held start late: every tile, the first included, is claimed
-    if (reclaim_mode) gl.static_first = 0;
+    if (reclaim_mode && gl.kind == 2) {
+        gl.static_first = 0;
+        const int64_t tiles = gl.num_m * gl.num_n;
+        gl.grid = (int)(tiles < ds.sm_count ? tiles : ds.sm_count);
+    }
     if ((e = cudaEventRecord(ev0, reclaim_mode ? sc_first : s0)) != cudaSuccess)
         return set_cuda_error(e, "event record");
     if (serial) {
