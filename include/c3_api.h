@@ -367,10 +367,13 @@ typedef struct {
  *   mode C3_MODE_CONCURRENT_SM_RECLAIM (sm_split >= 1): SM partitioning with
  *     reclaim -- the collective is launched first on sm_split SMs it holds
  *     alone, on the library's highest-priority stream so that its CTAs are
- *     dispatched before the GEMM's, the GEMM on every SM; the GEMM CTAs that
- *     find no free SM start as soon as the collective's SMs free up and, since
- *     the GEMM claims its tiles dynamically, take only the tiles still left.
- *     The partition lasts as long as the collective, not as long as the GEMM.
+ *     dispatched before the GEMM's.  The GEMM's tiles are planned for the SM
+ *     count - sm_split SMs it starts on, and it is launched on up to every
+ *     SM: the GEMM CTAs that find no free SM start as soon as the
+ *     collective's SMs free up and, since the GEMM claims its tiles
+ *     dynamically, take only the tiles still left (none, when the tiles fit
+ *     one wave on the SMs it started on).  The partition lasts as long as the
+ *     collective, not as long as the GEMM.
  *     priority has no further effect in this mode.
  *   In both partitioned modes the collective is one launch group of SM-count
  *   CTAs: its first sm_split CTAs, launched before the GEMM, and the rest,
