@@ -236,6 +236,36 @@ def test_partitioned_allreduce_bit_exact(c3, nranks, count, split, l2):
     assert (np.abs(dC.cpu().numpy().astype(np.float64) - C_ref) <= TOL * S_ref).all()
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 28672, 1024), (2048, 4096, 512)])
+def test_reclaim_plans_the_gemm_for_the_sms_it_starts_on(c3, M, N, K):
+    """Reclaim plans the GEMM's tiles for the SM count - sm_split SMs it starts
+    on, as a partition does, and launches up to every SM: min(tiles, SM count)
+    CTAs.  The memory-bound shape then fits one wave on the free SMs; a shape of
+    many waves keeps every SM.  The output stays within the tolerance."""
+    info = c3.c3_get_device_info()
+    split = 16
+    bn, msub, _ = c3.c3_gemm_plan(M, N, K, info["sm_count"] - split)
+    tiles = -(-M // (128 * msub)) * -(-N // bn)
+    A = I.bf16_uniform(51, (M, K))
+    B = I.bf16_uniform(52, (N, K))
+    dA = torch.from_numpy(A.view(np.int16)).cuda()
+    dB = torch.from_numpy(B.view(np.int16)).cuda()
+    dC = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    unit = 1 << 20
+    shards = [torch.randint(0, 256, (unit,), dtype=torch.uint8, device="cuda") for _ in range(8)]
+    out = torch.zeros(8 * unit, dtype=torch.uint8, device="cuda")
+    p = c3.Problem(dA, dB, dC, M, N, K, c3.C3_COLL_ALLGATHER, out, unit, 8, shards=shards)
+    t = c3.c3_run(p, 4, split, 0)
+    assert t["status"] == 0
+    assert t["gemm_ctas"] == min(tiles, info["sm_count"]), (t["gemm_ctas"], tiles)
+    assert t["smid_overlap"] == 0, t
+    assert torch.equal(out, torch.cat(shards))
+    rows = np.array([0, M // 2, M - 1])
+    C_ref, S_ref = oracle.gemm(A[rows], B)
+    got = dC[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    assert (np.abs(got - C_ref) <= TOL * S_ref).all()
+
+
 def test_copy_work_counters_recycle_over_many_launches(c3):
     """More collective launches than work-counter slots (64), with launch
     groups of 1..7 CTAs: a counter left non-zero would make a later launch
